@@ -1,0 +1,291 @@
+/*
+ * pcg_oracle.c -- plain, slow, obviously-correct fp64 CPU oracle for the
+ * particle-to-grid deposit path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no code, header or constant with the CUDA library.
+ *
+ * Every floating-point quantity is double.  Inputs arrive as float and are
+ * promoted exactly.  Compile with -ffp-contract=off so that each operation is
+ * rounded on its own (the 1D window test below is an integer decision taken in
+ * fp64; the CUDA side takes it with the same sequence of rounded operations).
+ *
+ * Sources (page title, section / equation):
+ *  - "03. Compaction and scatter-add" (WEANJ examples), sections "The problem"
+ *    and "Code": the 1D windowed cloud-in-cell histogram and its loss.
+ *  - "Mass Matrix Assembly on Tensor Cores for Implicit Particle-In-Cell
+ *    Methods" (Pennati & Markidis), Sec. 2.1 Eqs. (4)-(6) (mass matrix and the
+ *    rotation-response tensor), Sec. 2.3 Eq. (12) (tensor-product B-spline
+ *    shape, TSC base-offset rule), Sec. 3.4 (offset-indexed stencil storage).
+ *  - "Tiled current deposit" (Entity wiki), sections "How a tile deposit runs"
+ *    and "The tile-based spatial sort": tile counts ceil(n/T) per axis, tile
+ *    key, tile_offsets prefix sum.
+ *
+ * Parity pins: every function here is pinned by the CPU tests against brute
+ * force, closed forms or invariants (see tests/test_oracle_pins.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_VERSION 1
+
+int oracle_version(void) { return ORACLE_VERSION; }
+
+/* Julia's mod(j, n) for n > 0: result in [0, n). */
+static int64_t mod_floor(int64_t j, int64_t n) {
+    int64_t r = j % n;
+    return r < 0 ? r + n : r;
+}
+
+/* Periodic minimum image on the unit interval: d - round(d), ties to even
+ * (the JAX helper on the WEANJ page uses jnp.round). */
+static double minimg(double d) { return d - nearbyint(d); }
+
+/* ------------------------------------------------------------------------ */
+/* 1D windowed CIC histogram ("03. Compaction and scatter-add", "Code")       */
+/* ------------------------------------------------------------------------ */
+/*
+ * For t = 1..nsteps: c = t/nsteps, x = wrap(x0 + v*(t*dt)),
+ * d = minimg(x - c); particles with |d| < hw are deposited with weight
+ * w = (1 - |d|/hw)^2 and linear CIC weights on g = x*nb - 1/2 into bins
+ * j mod nb and (j+1) mod nb.  loss = sum_b (H_b - target_b)^2.
+ * H (double[nbins]) is overwritten.  Returns the number of (particle, step)
+ * deposits made.
+ */
+int64_t oracle_cic1d(const float *x0, const float *v, int64_t n,
+                     const float *target, int32_t nbins, int32_t nsteps,
+                     double dt, double hw, double *H, double *loss) {
+    int64_t nsel = 0;
+    for (int32_t b = 0; b < nbins; ++b) H[b] = 0.0;
+    for (int32_t t = 1; t <= nsteps; ++t) {
+        double c = (double)t / (double)nsteps;      /* window centre */
+        double s = (double)t * dt;                  /* elapsed time  */
+        for (int64_t p = 0; p < n; ++p) {
+            double xu = (double)x0[p] + (double)v[p] * s;
+            double x = xu - floor(xu);                 /* wrap to [0,1) */
+            double d = minimg(x - c);
+            if (!(fabs(d) < hw)) continue;             /* window test   */
+            double u = 1.0 - fabs(d) / hw;
+            double w = u * u;                          /* taper         */
+            double g = x * (double)nbins - 0.5;        /* CIC position  */
+            double jf = floor(g);
+            double f = g - jf;
+            int64_t j = (int64_t)jf;
+            H[mod_floor(j, nbins)] += w * (1.0 - f);
+            H[mod_floor(j + 1, nbins)] += w * f;
+            ++nsel;
+        }
+    }
+    double L = 0.0;
+    for (int32_t b = 0; b < nbins; ++b) {
+        double e = H[b] - (double)target[b];
+        L += e * e;
+    }
+    *loss = L;
+    return nsel;
+}
+
+/* ------------------------------------------------------------------------ */
+/* 1D B-spline weights (Pennati & Markidis, Sec. 2.3, Eq. (12))              */
+/* ------------------------------------------------------------------------ */
+/* Order-1 B-spline (CIC): phi(s) = 1 - |s| on |s| <= 1. */
+static double bspline1(double s) {
+    double a = fabs(s);
+    return a < 1.0 ? 1.0 - a : 0.0;
+}
+
+/* Order-2 B-spline (TSC / quadratic): 3/4 - s^2 on |s| <= 1/2,
+ * (3/2 - |s|)^2 / 2 on 1/2 <= |s| <= 3/2. */
+static double bspline2(double s) {
+    double a = fabs(s);
+    if (a <= 0.5) return 0.75 - a * a;
+    if (a <= 1.5) return 0.5 * (1.5 - a) * (1.5 - a);
+    return 0.0;
+}
+
+/*
+ * Support of one axis: first node and the per-node weights.
+ * order 1: nodes i, i+1 (i = floor x).
+ * order 2: nodes i-1..i+1 when xi < 1/2, else i..i+2 (the base-offset rule of
+ * Sec. 2.3); weights are phi(x - node).
+ * Returns the number of support nodes.
+ */
+static int axis_support(int order, double x, int64_t *first, double wts[3]) {
+    double fi = floor(x);
+    double xi = x - fi;
+    int64_t i = (int64_t)fi;
+    if (order == 1) {
+        *first = i;
+        wts[0] = bspline1(x - (double)i);
+        wts[1] = bspline1(x - (double)(i + 1));
+        return 2;
+    }
+    int64_t base = (xi < 0.5) ? i - 1 : i;
+    *first = base;
+    for (int k = 0; k < 3; ++k) wts[k] = bspline2(x - (double)(base + k));
+    return 3;
+}
+
+/* A position is inside the periodic domain when 0 <= x < N (NaN is not). */
+static int in_domain(double x, int32_t N) { return x >= 0.0 && x < (double)N; }
+
+/* exported for the pin tests: the per-axis support of one coordinate */
+int oracle_axis_support(int32_t order, double x, int64_t *first, double *wts) {
+    if (order != 1 && order != 2) return -1;
+    return axis_support(order, x, first, wts);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Current deposit J^c_g = sum_p q_p v^c_p W(x_p - x_g)                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * dim = 2 or 3, order = 1 (CIC) or 2 (quadratic).  grid[0..dim) = (Nx, Ny[, Nz]).
+ * pos[0..dim) are positions in cell units; vel[0..3) always three components
+ * (in 2D, vz deposits Jz on the 2D stencil).  J is double[3][ncells] with the
+ * flattened node index (z*Ny + y)*Nx + x; it is overwritten.  Periodic on every
+ * axis.  Particles with a coordinate outside [0, N) (or NaN) are skipped and
+ * counted.  Returns that count.
+ */
+int64_t oracle_deposit_current(int32_t dim, const int32_t *grid, int32_t order,
+                               int64_t n, const float *const *pos,
+                               const float *const *vel, const float *q,
+                               double *J) {
+    int32_t Nx = grid[0], Ny = grid[1], Nz = (dim == 3) ? grid[2] : 1;
+    int64_t ncells = (int64_t)Nx * Ny * Nz;
+    memset(J, 0, sizeof(double) * 3 * (size_t)ncells);
+    int64_t n_invalid = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        double x = pos[0][p], y = pos[1][p], z = (dim == 3) ? (double)pos[2][p] : 0.0;
+        if (!in_domain(x, Nx) || !in_domain(y, Ny) || (dim == 3 && !in_domain(z, Nz))) {
+            ++n_invalid;
+            continue;
+        }
+        int64_t fx, fy, fz = 0;
+        double wx[3], wy[3], wz[3] = {1.0, 0.0, 0.0};
+        int sx = axis_support(order, x, &fx, wx);
+        int sy = axis_support(order, y, &fy, wy);
+        int sz = 1;
+        if (dim == 3) sz = axis_support(order, z, &fz, wz);
+        double qv[3];
+        for (int c = 0; c < 3; ++c) qv[c] = (double)q[p] * (double)vel[c][p];
+        for (int kz = 0; kz < sz; ++kz) {
+            int64_t gz = mod_floor(fz + kz, Nz);
+            for (int ky = 0; ky < sy; ++ky) {
+                int64_t gy = mod_floor(fy + ky, Ny);
+                for (int kx = 0; kx < sx; ++kx) {
+                    int64_t gx = mod_floor(fx + kx, Nx);
+                    double W = wx[kx] * wy[ky] * wz[kz];
+                    int64_t g = (gz * Ny + gy) * Nx + gx;
+                    for (int c = 0; c < 3; ++c) J[c * ncells + g] += qv[c] * W;
+                }
+            }
+        }
+    }
+    return n_invalid;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Rotation-response tensor (Pennati & Markidis, Sec. 2.1, Eq. (5))          */
+/* ------------------------------------------------------------------------ */
+/*
+ * alpha = (I - C(w) + w w^T) / (1 + |w|^2) with C(w) u = w x u, i.e.
+ * C = [[0,-w3,w2],[w3,0,-w1],[-w2,w1,0]].  alpha is row-major [i][j].
+ */
+void oracle_alpha(const double *w, double *alpha) {
+    double C[3][3] = {{0.0, -w[2], w[1]}, {w[2], 0.0, -w[0]}, {-w[1], w[0], 0.0}};
+    double n2 = w[0] * w[0] + w[1] * w[1] + w[2] * w[2];
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j) {
+            double I = (i == j) ? 1.0 : 0.0;
+            alpha[i * 3 + j] = (I - C[i][j] + w[i] * w[j]) / (1.0 + n2);
+        }
+}
+
+/* ------------------------------------------------------------------------ */
+/* ECSIM block mass matrix, first-order B-splines (Sec. 2.1 Eq. (6), 3.4)    */
+/* ------------------------------------------------------------------------ */
+/*
+ * M[g][o][i][j] = sum_p w_p alpha_p^{ij} W_pg W_pg',  g' = g + delta (mod N),
+ * delta in {-1,0,1}^3, o = (dz+1)*9 + (dy+1)*3 + (dx+1).  sigma = 1.
+ * grid = (Nx, Ny, Nz), each >= 3 so that the 27 offsets name distinct nodes.
+ * M is double[ncells][27][3][3], overwritten.  Out-of-domain particles are
+ * skipped and counted; the count is returned.
+ */
+int64_t oracle_mass_matrix(const int32_t *grid, int64_t n,
+                           const float *const *pos, const float *wq,
+                           const float *const *omega, double *M) {
+    int32_t Nx = grid[0], Ny = grid[1], Nz = grid[2];
+    int64_t ncells = (int64_t)Nx * Ny * Nz;
+    memset(M, 0, sizeof(double) * 243 * (size_t)ncells);
+    int64_t n_invalid = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        double x[3] = {pos[0][p], pos[1][p], pos[2][p]};
+        if (!in_domain(x[0], Nx) || !in_domain(x[1], Ny) || !in_domain(x[2], Nz)) {
+            ++n_invalid;
+            continue;
+        }
+        int64_t first[3];
+        double wt[3][3];
+        for (int mu = 0; mu < 3; ++mu) axis_support(1, x[mu], &first[mu], wt[mu]);
+        double om[3] = {omega[0][p], omega[1][p], omega[2][p]};
+        double alpha[9];
+        oracle_alpha(om, alpha);
+        double s[9];
+        for (int ij = 0; ij < 9; ++ij) s[ij] = (double)wq[p] * alpha[ij];
+        /* corner a = (ax, ay, az) in {0,1}^3 */
+        for (int a = 0; a < 8; ++a) {
+            int ax = a & 1, ay = (a >> 1) & 1, az = (a >> 2) & 1;
+            double Wa = wt[0][ax] * wt[1][ay] * wt[2][az];
+            int64_t g = (mod_floor(first[2] + az, Nz) * Ny + mod_floor(first[1] + ay, Ny)) * Nx
+                        + mod_floor(first[0] + ax, Nx);
+            for (int b = 0; b < 8; ++b) {
+                int bx = b & 1, by = (b >> 1) & 1, bz = (b >> 2) & 1;
+                double Wb = wt[0][bx] * wt[1][by] * wt[2][bz];
+                int o = (bz - az + 1) * 9 + (by - ay + 1) * 3 + (bx - ax + 1);
+                double *blk = M + ((size_t)g * 27 + (size_t)o) * 9;
+                for (int ij = 0; ij < 9; ++ij) blk[ij] += s[ij] * Wa * Wb;
+            }
+        }
+    }
+    return n_invalid;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Tile key and tile_offsets ("Tiled current deposit", tile-based sort)      */
+/* ------------------------------------------------------------------------ */
+/*
+ * ntiles per axis = ceil(N / tile); tile index of a particle = index of the
+ * tile holding its cell floor(x), x fastest.  Out-of-domain particles get the
+ * sentinel key ntiles_total.  offsets[0..ntiles_total] is the exclusive prefix
+ * sum of the per-tile counts (offsets[ntiles_total] = number of in-domain
+ * particles).  Returns ntiles_total.
+ */
+int64_t oracle_tile_keys(int32_t dim, const int32_t *grid, int32_t tile, int64_t n,
+                         const float *const *pos, uint32_t *keys, uint32_t *offsets) {
+    int64_t nt[3] = {1, 1, 1};
+    for (int mu = 0; mu < dim; ++mu) nt[mu] = (grid[mu] + tile - 1) / tile;
+    int64_t total = nt[0] * nt[1] * nt[2];
+    for (int64_t t = 0; t <= total; ++t) offsets[t] = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        int ok = 1;
+        int64_t tc[3] = {0, 0, 0};
+        for (int mu = 0; mu < dim; ++mu) {
+            double x = pos[mu][p];
+            if (!in_domain(x, grid[mu])) { ok = 0; break; }
+            tc[mu] = (int64_t)floor(x) / tile;
+        }
+        uint32_t k = ok ? (uint32_t)((tc[2] * nt[1] + tc[1]) * nt[0] + tc[0]) : (uint32_t)total;
+        if (keys) keys[p] = k;
+        if (ok) offsets[k] += 1;
+    }
+    /* exclusive scan in place */
+    uint32_t run = 0;
+    for (int64_t t = 0; t <= total; ++t) {
+        uint32_t c = offsets[t];
+        offsets[t] = run;
+        run += c;
+    }
+    return total;
+}

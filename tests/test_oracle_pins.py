@@ -1,0 +1,418 @@
+"""Pins of the fp64 CPU oracle to things other than itself.
+
+Each test checks the oracle against a brute-force formulation written
+differently (all-node sums with B-splines built from box convolutions, a dense
+W S W^T product, numpy bincount), a hand-worked fixture under tests/golden, a
+closed form, or an invariant of the method.  A dropped term, a wrong sign or a
+transposed index in the oracle fails at least one of them.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import read_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------------------
+# B-splines built from their definition: repeated convolution with the unit box
+# (Pennati & Markidis, Sec. 2.3, Eq. (12)).  phi_n(s) = int_{s-1/2}^{s+1/2} phi_{n-1}.
+# The antiderivative of the previous order is evaluated in closed form, so none
+# of the oracle's piecewise formulas or node-selection logic is reused here.
+# ---------------------------------------------------------------------------
+def _box_cdf(t):
+    return np.clip(t + 0.5, 0.0, 1.0)
+
+
+def _tent(s):  # order 1 = box * box
+    return _box_cdf(s + 0.5) - _box_cdf(s - 0.5)
+
+
+def _tent_cdf(t):  # integral of the tent from -inf to t
+    t = np.asarray(t, dtype=np.float64)
+    return np.where(t < -1, 0.0,
+           np.where(t < 0, 0.5 * (t + 1) ** 2,
+           np.where(t < 1, 1.0 - 0.5 * (1 - t) ** 2, 1.0)))
+
+
+def _quad(s):  # order 2 = tent * box
+    return _tent_cdf(s + 0.5) - _tent_cdf(s - 0.5)
+
+
+def _phi(order, s):
+    return _tent(s) if order == 1 else _quad(s)
+
+
+def _minimg(s, N):
+    return s - N * np.round(s / N)
+
+
+def test_bspline_from_convolution_matches_numeric_integral():
+    # the convolution construction itself, against a midpoint Riemann sum
+    s = np.linspace(-2, 2, 41)
+    h = 1e-4
+    t = np.arange(-3, 3, h) + h / 2
+    tent_num = np.array([np.sum((np.abs(t) <= 0.5) & (np.abs(x - t) <= 0.5)) * h for x in s])
+    assert np.allclose(tent_num, _tent(s), atol=2e-4)
+    quad_num = np.array([np.sum(_tent(t) * (np.abs(x - t) <= 0.5)) * h for x in s])
+    assert np.allclose(quad_num, _quad(s), atol=2e-4)
+
+
+@pytest.mark.parametrize("row", read_golden("bspline_weights.txt"))
+def test_axis_support_golden(row):
+    order, x, first = int(row[0]), float(row[1]), int(row[2])
+    want = [float(Fraction(w)) for w in row[3:]]
+    got_first, got_w = oracle.axis_support(order, x)
+    assert got_first == first
+    assert np.allclose(got_w, want, rtol=0, atol=1e-15)
+
+
+def test_axis_support_against_convolution_spline():
+    rng = np.random.default_rng(7)
+    for order in (1, 2):
+        for x in list(rng.uniform(0, 50, 200)) + [0.0, 0.5, 1.0, 7.5, 7.25]:
+            first, w = oracle.axis_support(order, x)
+            nodes = first + np.arange(len(w))
+            assert np.allclose(w, _phi(order, x - nodes), atol=1e-14)
+            # the support holds every node with a non-zero weight
+            around = np.arange(int(np.floor(x)) - 3, int(np.floor(x)) + 4)
+            outside = np.setdiff1d(around, nodes)
+            assert np.allclose(_phi(order, x - outside), 0.0, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# current deposit: brute force over every node of small periodic grids
+# ---------------------------------------------------------------------------
+def _brute_J(grid, order, pos, vel, q):
+    dim = len(grid)
+    shape = tuple(reversed(grid))
+    J = np.zeros((3,) + shape)
+    axes = np.meshgrid(*[np.arange(N) for N in reversed(grid)], indexing="ij")  # z,y,x order
+    node = list(reversed(axes))  # node[mu] has coordinate mu
+    for p in range(len(q)):
+        x = [float(pos[mu][p]) for mu in range(dim)]
+        if not all(0 <= x[mu] < grid[mu] for mu in range(dim)):
+            continue
+        W = np.ones(shape)
+        for mu in range(dim):
+            W = W * _phi(order, _minimg(x[mu] - node[mu], grid[mu]))
+        for c in range(3):
+            J[c] += float(q[p]) * float(vel[c][p]) * W
+    return J
+
+
+def _small_particles(rng, grid, n):
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    # special positions: on nodes, on half-cells, next to the upper edge, at 0
+    for mu, N in enumerate(grid):
+        pos[mu][0] = 0.0
+        pos[mu][1] = np.float32(N) - np.float32(2 ** -20)
+        pos[mu][2] = 1.5
+        pos[mu][3] = 2.0
+    vel = [rng.normal(0, 0.3, n).astype(np.float32) for _ in range(3)]
+    q = rng.choice([-1.0, 1.0, 0.5], n).astype(np.float32)
+    return pos, vel, q
+
+
+@pytest.mark.parametrize("grid", [(5, 4), (3, 7), (4, 5, 3), (6, 3, 4)])
+@pytest.mark.parametrize("order", [1, 2])
+def test_deposit_bruteforce_all_nodes(grid, order):
+    rng = np.random.default_rng(hash((grid, order)) % 2 ** 32)
+    pos, vel, q = _small_particles(rng, grid, 24)
+    J, ninv = oracle.deposit_current(grid, order, pos, vel, q)
+    assert ninv == 0
+    Jb = _brute_J(grid, order, pos, vel, q)
+    scale = np.abs(Jb).max()
+    assert np.abs(J - Jb).max() <= 1e-12 * scale
+
+
+@pytest.mark.parametrize("order", [1, 2])
+def test_deposit_partition_of_unity_and_moments(order):
+    grid = (9, 8, 7)
+    rng = np.random.default_rng(11)
+    n = 500
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    vel = [rng.normal(0, 0.2, n).astype(np.float32) for _ in range(3)]
+    q = rng.choice([-1.0, 1.0], n).astype(np.float32)
+    J, _ = oracle.deposit_current(grid, order, pos, vel, q)
+    for c in range(3):
+        want = np.sum(q.astype(np.float64) * vel[c].astype(np.float64))
+        assert abs(J[c].sum() - want) <= 1e-11 * max(1.0, np.abs(q * vel[c]).sum())
+    # single particle: first moment zero, second moment = variance of the spline
+    for x in [(3.3, 4.71, 2.05), (0.2, 7.9, 6.5), (4.0, 4.0, 4.0)]:
+        J1, _ = oracle.deposit_current(grid, order, [np.array([v], np.float32) for v in x],
+                                       [np.array([1.0], np.float32), np.zeros(1, np.float32), np.zeros(1, np.float32)],
+                                       np.ones(1, np.float32))
+        W = J1[0]  # (z, y, x)
+        xs = [float(np.float32(v)) for v in x]
+        for mu, N in enumerate(grid):
+            axis = 2 - mu
+            marg = W.sum(axis=tuple(a for a in range(3) if a != axis))
+            d = _minimg(np.arange(N) - xs[mu], N)
+            assert abs((marg * d).sum()) < 1e-12
+            if order == 2:
+                assert abs((marg * d * d).sum() - 0.25) < 1e-12
+            else:
+                xi = xs[mu] - np.floor(xs[mu])
+                assert abs((marg * d * d).sum() - xi * (1 - xi)) < 1e-12
+
+
+def test_deposit_node_closed_forms():
+    grid = (6, 6, 6)
+    one = np.ones(1, np.float32)
+    z = np.zeros(1, np.float32)
+    # CIC on a node: all weight on that node
+    J, _ = oracle.deposit_current(grid, 1, [np.array([2.0], np.float32)] * 3, [one, z, z], one)
+    assert J[0][2, 2, 2] == 1.0 and np.count_nonzero(J[0]) == 1
+    # quadratic on a node: 1/8, 3/4, 1/8 per axis
+    J, _ = oracle.deposit_current(grid, 2, [np.array([2.0], np.float32)] * 3, [one, z, z], one)
+    w = np.array([1 / 8, 3 / 4, 1 / 8])
+    assert np.allclose(J[0][1:4, 1:4, 1:4], np.einsum("i,j,k->ijk", w, w, w), atol=1e-15)
+    assert np.count_nonzero(J[0]) == 27
+
+
+def test_deposit_invalid_particles_skipped_and_counted():
+    grid = (4, 4)
+    pos = [np.array([1.5, 4.0, -0.25, np.nan, 2.5], np.float32),
+           np.array([1.5, 1.0, 1.0, 1.0, 3.99], np.float32)]
+    vel = [np.ones(5, np.float32)] * 3
+    q = np.ones(5, np.float32)
+    J, ninv = oracle.deposit_current(grid, 1, pos, vel, q)
+    assert ninv == 3
+    Jv, _ = oracle.deposit_current(grid, 1, [p[[0, 4]] for p in pos], [v[[0, 4]] for v in vel], q[[0, 4]])
+    assert np.array_equal(J, Jv)
+
+
+# ---------------------------------------------------------------------------
+# 1D windowed CIC histogram
+# ---------------------------------------------------------------------------
+def _golden_cic1d():
+    rows = {r[0]: r[1:] for r in read_golden("cic1d_worked.txt")}
+    f = lambda k: [float(v) for v in rows[k]]
+    return rows, f
+
+
+def test_cic1d_worked_example():
+    rows, f = _golden_cic1d()
+    H, loss, nsel = oracle.cic1d(np.array(f("x0"), np.float32), np.array(f("v"), np.float32),
+                                 np.array(f("target"), np.float32), nbins=int(rows["nbins"][0]),
+                                 nsteps=int(rows["nsteps"][0]), dt=f("dt")[0], halfwidth=f("halfwidth")[0])
+    want = np.array(f("H_num")) / f("H_den")[0]
+    assert np.allclose(H, want, rtol=0, atol=1e-15)
+    assert abs(loss - f("loss_num")[0] / f("loss_den")[0]) < 1e-15
+    assert nsel == int(rows["n_deposits"][0])
+
+
+def _tent_hist(x, w, nb):
+    """Histogram by the periodic tent at bin centres (b + 1/2)/nb: no floor, no mod."""
+    b = (np.arange(nb) + 0.5) / nb
+    d = x[:, None] - b[None, :]
+    d = d - np.round(d)
+    return (w[:, None] * np.maximum(0.0, 1.0 - np.abs(d) * nb)).sum(0)
+
+
+def test_cic1d_all_selected_matches_tent_bruteforce():
+    # a half-width above 1/2 selects every particle at every step (|minimg| <= 1/2)
+    rng = np.random.default_rng(3)
+    n, nb, T, dt, h = 40, 16, 7, 0.013, 0.8
+    x0 = rng.random(n).astype(np.float32)
+    v = rng.normal(0, 0.3, n).astype(np.float32)
+    target = rng.random(nb).astype(np.float32)
+    H, loss, nsel = oracle.cic1d(x0, v, target, nb, T, dt, h)
+    assert nsel == n * T
+    Hb = np.zeros(nb)
+    for t in range(1, T + 1):
+        x = np.mod(x0.astype(np.float64) + v.astype(np.float64) * (t * dt), 1.0)
+        r = np.mod(x - t / T, 1.0)
+        dist = np.minimum(r, 1.0 - r)            # circular distance to the window centre
+        Hb += _tent_hist(x, (1.0 - dist / h) ** 2, nb)
+    assert np.allclose(H, Hb, rtol=0, atol=1e-12)
+    assert abs(loss - np.sum((Hb - target.astype(np.float64)) ** 2)) < 1e-10
+
+
+def test_cic1d_selection_count_and_mass():
+    d = synth.cic1d()
+    H, loss, nsel = oracle.cic1d(d["x0"], d["v"], d["target"], d["nbins"], d["nsteps"], d["dt"], d["halfwidth"])
+    # independent count of (particle, step) pairs inside the window: circular distance
+    x0 = d["x0"].astype(np.float64)
+    v = d["v"].astype(np.float64)
+    tot_w = 0.0
+    cnt = 0
+    per_step = []
+    ever = np.zeros(x0.size, bool)
+    for t in range(1, d["nsteps"] + 1):
+        x = np.mod(x0 + v * (t * d["dt"]), 1.0)
+        r = np.mod(x - t / d["nsteps"], 1.0)
+        dist = np.minimum(r, 1.0 - r)
+        sel = dist < d["halfwidth"] * (1 - 1e-9)
+        near = np.abs(dist - d["halfwidth"]) < 1e-12
+        assert not near.any()  # no pair sits on the window edge for this seed
+        cnt += sel.sum()
+        per_step.append(sel.sum())
+        ever |= sel
+        tot_w += ((1 - dist[sel] / d["halfwidth"]) ** 2).sum()
+    assert nsel == cnt
+    assert abs(H.sum() - tot_w) < 1e-9                # CIC weights sum to one
+    assert (H >= 0).all()
+    # loose sanity check of the generator against the page's printed statistics
+    # (capacity 30 and 983 of 2000 particles ever selected, other inputs): same regime
+    assert 15 <= max(per_step) <= 45
+    assert 0.35 <= ever.mean() <= 0.65
+
+
+# ---------------------------------------------------------------------------
+# mass matrix: dense W S W^T on tiny grids, alpha closed forms and invariants
+# ---------------------------------------------------------------------------
+def _cross_matrix(w):
+    return np.array([[0, -w[2], w[1]], [w[2], 0, -w[0]], [-w[1], w[0], 0]], dtype=np.float64)
+
+
+@pytest.mark.parametrize("row", read_golden("alpha_closed_form.txt"))
+def test_alpha_closed_form(row):
+    vals = [float(v) for v in row]
+    a = oracle.alpha(vals[:3])
+    assert np.allclose(a, np.array(vals[3:]).reshape(3, 3), atol=1e-15)
+
+
+def test_alpha_is_inverse_of_one_plus_cross():
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        w = rng.normal(0, 1.5, 3)
+        a = oracle.alpha(w)
+        want = np.linalg.solve(np.eye(3) + _cross_matrix(w), np.eye(3))
+        assert np.allclose(a, want, atol=1e-13)
+        # the cross operator really is w x u
+        u = rng.normal(size=3)
+        assert np.allclose(_cross_matrix(w) @ u, np.cross(w, u))
+
+
+def _dense_mass(grid, pos, wq, omega):
+    """M^{ij} = W S^{ij} W^T with W the dense node-by-particle weight matrix (Eq. (10))."""
+    Nx, Ny, Nz = grid
+    ng = Nx * Ny * Nz
+    n = len(wq)
+    gz, gy, gx = np.meshgrid(np.arange(Nz), np.arange(Ny), np.arange(Nx), indexing="ij")
+    W = np.zeros((ng, n))
+    for p in range(n):
+        Wp = (_tent(_minimg(float(pos[0][p]) - gx, Nx)) * _tent(_minimg(float(pos[1][p]) - gy, Ny))
+              * _tent(_minimg(float(pos[2][p]) - gz, Nz)))
+        W[:, p] = Wp.ravel()
+    S = np.zeros((3, 3, n))
+    for p in range(n):
+        w = np.array([float(omega[c][p]) for c in range(3)])
+        a = np.linalg.solve(np.eye(3) + _cross_matrix(w), np.eye(3))   # Eq. (5) in closed form
+        S[:, :, p] = float(wq[p]) * a
+    Md = np.einsum("gp,ijp,hp->ijgh", W, S, W)
+    return Md  # [i][j][g][g']
+
+
+def _offset_layout(Md, grid):
+    Nx, Ny, Nz = grid
+    ng = Nx * Ny * Nz
+    out = np.zeros((ng, 27, 3, 3))
+    for g in range(ng):
+        x, y, z = g % Nx, (g // Nx) % Ny, g // (Nx * Ny)
+        for dz in (-1, 0, 1):
+            for dy in (-1, 0, 1):
+                for dx in (-1, 0, 1):
+                    h = (((z + dz) % Nz) * Ny + (y + dy) % Ny) * Nx + (x + dx) % Nx
+                    o = (dz + 1) * 9 + (dy + 1) * 3 + (dx + 1)
+                    out[g, o] = Md[:, :, g, h]
+    return out
+
+
+@pytest.mark.parametrize("grid", [(3, 4, 5), (4, 3, 3), (5, 5, 4)])
+def test_mass_matrix_dense_product(grid):
+    rng = np.random.default_rng(sum(grid))
+    n = 30
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    pos[0][0] = np.float32(grid[0]) - np.float32(1e-5)  # wraps in x
+    pos[1][1] = 0.0
+    wq = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    omega = [rng.normal(0, 0.6, n).astype(np.float32) for _ in range(3)]
+    M, ninv = oracle.mass_matrix(grid, pos, wq, omega)
+    assert ninv == 0
+    want = _offset_layout(_dense_mass(grid, pos, wq, omega), grid)
+    got = M.reshape(-1, 27, 3, 3)
+    assert np.abs(got - want).max() <= 1e-12 * np.abs(want).max()
+
+
+def test_mass_matrix_invariants():
+    grid = (6, 5, 4)
+    Nx, Ny, Nz = grid
+    rng = np.random.default_rng(9)
+    n = 400
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    wq = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    omega = [rng.normal(0, 0.7, n).astype(np.float32) for _ in range(3)]
+    M, _ = oracle.mass_matrix(grid, pos, wq, omega)
+    M = M.reshape(-1, 27, 3, 3)
+    # symmetry per component (Eq. (11)): M[g][delta] = M[g+delta][-delta]
+    for g in range(M.shape[0]):
+        x, y, z = g % Nx, (g // Nx) % Ny, g // (Nx * Ny)
+        for o in range(27):
+            dx, dy, dz = o % 3 - 1, (o // 3) % 3 - 1, o // 9 - 1
+            h = (((z + dz) % Nz) * Ny + (y + dy) % Ny) * Nx + (x + dx) % Nx
+            assert np.allclose(M[g, o], M[h, 26 - o], atol=1e-13)
+    # row sums = deposited weight sum_p s_p W_pg; total = sum_p s_p
+    s = np.stack([float(wq[p]) * oracle.alpha([float(omega[c][p]) for c in range(3)]) for p in range(n)])
+    gz, gy, gx = np.meshgrid(np.arange(Nz), np.arange(Ny), np.arange(Nx), indexing="ij")
+    dep = np.zeros((M.shape[0], 3, 3))
+    for p in range(n):
+        Wp = (_tent(_minimg(float(pos[0][p]) - gx, Nx)) * _tent(_minimg(float(pos[1][p]) - gy, Ny))
+              * _tent(_minimg(float(pos[2][p]) - gz, Nz)))
+        dep += Wp.ravel()[:, None, None] * s[p][None]
+    assert np.allclose(M.sum(axis=1), dep, atol=1e-12)
+    assert np.allclose(M.sum(axis=(0, 1)), s.sum(0), atol=1e-10)
+
+
+def test_mass_matrix_closed_forms():
+    grid = (4, 4, 4)
+    one = np.ones(1, np.float32)
+    zero = np.zeros(1, np.float32)
+    # cell-centre particle, omega = 0: every one of the 64 pairs gets w/64 * I
+    M, _ = oracle.mass_matrix(grid, [np.array([1.5], np.float32)] * 3, np.array([2.0], np.float32), [zero] * 3)
+    M = M.reshape(-1, 27, 3, 3)
+    nz = np.argwhere(np.abs(M[..., 0, 0]) > 0)
+    assert len(nz) == 64
+    for g, o in nz:
+        assert np.allclose(M[g, o], 2.0 / 64 * np.eye(3), atol=1e-16)
+    # particle on a node with omega = (0, 0, 1/2): one block, w * alpha, at offset 13
+    M, _ = oracle.mass_matrix(grid, [np.array([2.0], np.float32)] * 3, one,
+                              [zero, zero, np.array([0.5], np.float32)])
+    M = M.reshape(-1, 27, 3, 3)
+    g = (2 * 4 + 2) * 4 + 2
+    assert np.allclose(M[g, 13], [[0.8, 0.4, 0], [-0.4, 0.8, 0], [0, 0, 1]], atol=1e-15)
+    assert np.count_nonzero(M) == 5
+
+
+# ---------------------------------------------------------------------------
+# tile keys and tile_offsets
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("grid,tile", [((16, 16), 8), ((20, 13), 8), ((12, 10, 9), 4), ((16, 16, 16), 8), ((7, 5, 6), 1)])
+def test_tile_keys_against_bincount(grid, tile):
+    rng = np.random.default_rng(len(grid) * 100 + tile)
+    n = 3000
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    pos[0][:3] = [np.nan, -1.0, float(grid[0])]
+    keys, offs = oracle.tile_keys(grid, tile, pos)
+    nt = [-(-N // tile) for N in grid]
+    tc = [np.floor(np.nan_to_num(p, nan=-1.0)).astype(np.int64) // tile for p in pos]
+    ok = np.ones(n, bool)
+    for mu, N in enumerate(grid):
+        ok &= (pos[mu] >= 0) & (pos[mu] < N)
+    k = np.zeros(n, np.int64)
+    stride = 1
+    for mu in range(len(grid)):
+        k += np.where(ok, tc[mu], 0) * stride
+        stride *= nt[mu]
+    total = stride
+    k[~ok] = total
+    assert np.array_equal(keys, k.astype(np.uint32))
+    counts = np.bincount(k, minlength=total + 1)[:total]
+    assert np.array_equal(offs, np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32))
+    assert offs[-1] == ok.sum()
