@@ -1,0 +1,231 @@
+/*
+ * pcg.h -- C ABI of the GB300 (sm_103a) particle-to-grid deposit library.
+ *
+ * One shared library, libpcg.so.  Every entry point:
+ *   - takes plain pointers and sizes (no framework types);
+ *   - unless stated otherwise, data pointers are DEVICE pointers owned by the
+ *     caller, and "const T* const* name" parameters are HOST arrays holding
+ *     device pointers (one per axis / component / payload field);
+ *   - enqueues its kernels on `stream` (a cudaStream_t passed as void*; NULL
+ *     selects the legacy default stream) and returns without synchronising;
+ *   - validates its arguments on the host before launching anything and
+ *     returns a pcg_status; on any error nothing is enqueued;
+ *   - OVERWRITES its outputs (never accumulates into them), except `stats`,
+ *     whose counters are added to;
+ *   - never allocates device memory: scratch space is a caller-provided
+ *     `workspace` whose size is returned by the matching *_workspace_size query
+ *     (a NULL workspace with size 0 is fine where that query returns 0).
+ *
+ * Conventions.  Positions are in cell units, x in [0, N) per axis; node g sits at
+ * integer coordinates and cell i is [i, i+1).  Grids are periodic on every
+ * axis.  Arrays over nodes or cells are flattened with x fastest:
+ * index = (z * Ny + y) * Nx + x.  Particle arrays are structure-of-arrays fp32.
+ * A particle with a coordinate outside [0, N) or NaN is "invalid": it is skipped
+ * and counted in stats->n_invalid.
+ */
+#ifndef PCG_H
+#define PCG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PCG_API __attribute__((visibility("default")))
+#else
+#define PCG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pcg_status {
+    PCG_OK = 0,
+    PCG_ERR_INVALID_ARG = 1, /* null pointer, bad size, unsupported value   */
+    PCG_ERR_WORKSPACE = 2,   /* workspace smaller than the size query says  */
+    PCG_ERR_UNSUPPORTED = 3, /* valid request without a compiled kernel     */
+    PCG_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed        */
+    PCG_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up */
+    PCG_ERR_DOMAIN = 6       /* data-dependent anomaly reported in stats    */
+} pcg_status;
+
+/* Device-resident counters, caller-owned; every call ADDS to them.  Zero the
+ * struct before the calls whose anomalies you want to count, copy it to the
+ * host after synchronising the stream, and map it with pcg_stats_check(). */
+typedef struct pcg_stats {
+    unsigned long long n_escaped; /* particles deposited through the escape valve */
+    unsigned long long n_invalid; /* particles skipped: position outside [0, N) or NaN */
+    unsigned int error_flags;     /* bit set of PCG_FLAG_* */
+    unsigned int reserved;
+} pcg_stats;
+
+#define PCG_FLAG_BAD_LAYOUT 1u /* tile_offsets / cell_offsets not monotone or out of range */
+#define PCG_FLAG_CELL_MISMATCH 2u /* mass matrix: a particle not inside the cell it is listed under */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+PCG_API int pcg_version(void);
+
+/* Static, NUL-terminated description of a status code. */
+PCG_API const char *pcg_status_string(int status);
+
+/* Map a HOST copy of a pcg_stats to PCG_OK or PCG_ERR_DOMAIN (any invalid
+ * particle or error flag).  Escapes are normal and do not count as errors. */
+PCG_API pcg_status pcg_stats_check(const pcg_stats *host_stats);
+
+/* -------------------------------------------------------------------------
+ * 1D windowed cloud-in-cell histogram and its loss.
+ * Defined by "03. Compaction and scatter-add" (WEANJ examples), sections
+ * "The problem" and "Code" (the loop over t = 1..T with the window test, the
+ * taper and the two scatter-adds), and the JAX helpers minimg / taper on the
+ * same page.
+ *
+ * For t = 1..nsteps: c = t/nsteps; x = wrap(x0 + v*(t*dt)) in [0,1);
+ * d = x - c - round(d) (periodic minimum image, ties to even); if |d| < halfwidth
+ * the particle adds w = (1 - |d|/halfwidth)^2 times the linear CIC weights of
+ * g = x*nbins - 1/2 to bins floor(g) mod nbins and floor(g)+1 mod nbins.
+ * loss = sum_b (H_b - target_b)^2.
+ *
+ * The window test, g and floor(g) are evaluated in fp64 with individually
+ * rounded operations (no fused multiply-add); the deposits are added in fp32
+ * and the loss is accumulated in fp64 from the fp32 histogram.
+ *
+ *   x0, v    device float[n]: initial positions on [0,1) (any finite value is
+ *            wrapped) and velocities.
+ *   target   device float[nbins].
+ *   H        device float[nbins], output (overwritten).
+ *   loss     device double[1], output (overwritten).
+ *   n >= 0; 1 <= nbins <= 16384; nsteps >= 1; 0 < halfwidth; dt finite.
+ * One launch of one 8-CTA thread-block cluster; no workspace.
+ */
+PCG_API pcg_status pcg_deposit_cic1d(const float *x0, const float *v, int64_t n, const float *target,
+                             int32_t nbins, int32_t nsteps, double dt, double halfwidth,
+                             float *H, double *loss, void *stream);
+
+/* -------------------------------------------------------------------------
+ * Tile counting sort.
+ * Defined by "Tiled current deposit" (Entity wiki), section "The tile-based
+ * spatial sort" (tile counts ntiles = ceil(N / T) per axis, a per-particle tile
+ * key, invalid particles in a sentinel bin after the last tile, the
+ * tile_offsets prefix sum, SoA members physically permuted into tile order)
+ * and section "How a tile deposit runs" (tile t owns
+ * [tile_offsets[t], tile_offsets[t+1])).  With tile = 1 the sort orders
+ * particles by cell, the order the mass-matrix assembly assumes (Pennati &
+ * Markidis, Sec. 3.1).
+ *
+ * key of a particle = index of the tile holding cell floor(key_pos), x fastest;
+ * n_tiles = prod_mu ceil(grid[mu] / tile).  Invalid key positions go to the
+ * sentinel bin n_tiles.
+ *
+ *   dim        2 or 3.  grid: HOST int32[dim], each in [1, 2^20], and the total
+ *              node count below 2^31.
+ *   tile       1..64.  n_tiles + 1 must stay below 2^31.
+ *   n          number of particles, 0 <= n < 2^32 - 1.
+ *   key_pos    HOST array of dim device float[n]: positions defining the key
+ *              (for example the sort-time / previous positions).
+ *   n_payload  1..16 arrays of 4-byte elements (fp32, int32 or uint32 bits).
+ *   payload_in / payload_out   HOST arrays of n_payload device pointers to n
+ *              elements each; payload_out[k] receives payload_in[k] permuted
+ *              into tile order.  Outputs must not overlap any input.  A
+ *              key_pos array may also appear among payload_in.
+ *   tile_offsets  device uint32[n_tiles + 1], output: tile t holds slots
+ *              [tile_offsets[t], tile_offsets[t+1]); invalid particles fill
+ *              [tile_offsets[n_tiles], n).  Order inside a tile is unspecified.
+ *   stats      device pcg_stats or NULL; n_invalid counts the sentinel bin.
+ *   workspace  device memory of at least pcg_tile_sort_workspace_size() bytes,
+ *              256-byte aligned; contents on entry are irrelevant.
+ * Launches: 3 (bin count <= 32769, block-privatised counts) or 4 otherwise.
+ */
+PCG_API pcg_status pcg_tile_sort_workspace_size(int32_t dim, const int32_t *grid, int32_t tile, int64_t n,
+                                        size_t *bytes);
+PCG_API pcg_status pcg_tile_sort(int32_t dim, const int32_t *grid, int32_t tile, int64_t n,
+                         const float *const *key_pos, int32_t n_payload,
+                         const void *const *payload_in, void *const *payload_out,
+                         uint32_t *tile_offsets, pcg_stats *stats, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* -------------------------------------------------------------------------
+ * Current deposit J^c_g = sum_p q_p v^c_p W(x_p - x_g), c in {x, y, z}.
+ * Defined by the tensor-product B-spline shape of Pennati & Markidis, Sec. 2.3,
+ * Eq. (12) (order 1 = cloud-in-cell, 2 nodes per axis; order 2 = quadratic,
+ * nodes {j-1, j, j+1} when the fractional coordinate is below 1/2, else
+ * {j, j+1, j+2}), deposited as in "Tiled current deposit" (Entity wiki),
+ * sections "How a tile deposit runs" (one team per tile, a haloed
+ * (T + 2*HALO)^D x 3 scratch tile, the fit test, a single flush per scratch
+ * cell), "Halo sizing" (HALO = stencil reach + drift budget) and "Correctness
+ * is independent of the halo" (a particle whose stencil leaves the scratch
+ * window is deposited whole into J through global atomics).
+ *
+ *   dim        2 or 3 (in 2D the stencil is 2D and vel[2] deposits Jz).
+ *   grid       HOST int32[dim], each >= 1.
+ *   order      1 or 2.
+ *   tile       4 or 8 (the tiled kernels compiled in); ignored when
+ *              tile_offsets is NULL.
+ *   halo       0, 1 or 2 cells per side; correctness never depends on it.
+ *   block      threads per CTA: 0 = automatic, else 128, 256 or 512.
+ *   n          number of particles.
+ *   pos        HOST array of dim device float[n]: deposit positions.
+ *   vel        HOST array of 3 device float[n].
+ *   q          device float[n], charges.
+ *   tile_offsets  NULL: flat path, one thread per particle straight to global
+ *              atomics.  Else device uint32[n_tiles + 1] from pcg_tile_sort
+ *              with the same dim, grid and tile: particles of tile t are
+ *              [tile_offsets[t], tile_offsets[t+1]) and may have moved since the
+ *              sort (drift); slots [tile_offsets[n_tiles], n) are deposited by
+ *              the flat path (the tail pass).
+ *   J          device float[3][ncells], output (overwritten).
+ *   stats      device pcg_stats or NULL: n_escaped, n_invalid, error_flags.
+ *   workspace  device memory of pcg_deposit_current_workspace_size() bytes.
+ * Launches: 2 (flat) or 3 (tiled).
+ */
+PCG_API pcg_status pcg_deposit_current_workspace_size(int32_t dim, const int32_t *grid, int32_t tile,
+                                              int64_t n, size_t *bytes);
+PCG_API pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int32_t order, int32_t tile,
+                               int32_t halo, int32_t block, int64_t n, const float *const *pos,
+                               const float *const *vel, const float *q,
+                               const uint32_t *tile_offsets, float *J, pcg_stats *stats,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* -------------------------------------------------------------------------
+ * ECSIM block mass matrix with first-order (CIC) B-splines.
+ * Defined by Pennati & Markidis, Sec. 2.1, Eqs. (4)-(6):
+ *   M^{ij}_{g g'} = sum_p s_p^{ij} W_pg W_pg',  s_p = w_p alpha_p,
+ *   alpha_p = (I - C(omega_p) + omega_p omega_p^T) / (1 + |omega_p|^2),
+ *   C(omega) u = omega x u,
+ * with every constant prefactor absorbed into w (sigma = 1), assembled cell by
+ * cell as in Sec. 3.1-3.2, Eqs. (14)-(20) (A = W S^{ij}, B = W^T over batches of
+ * particles, accumulated in place), and stored by stencil offset as in Sec. 3.4
+ * with all 27 offsets kept.
+ *
+ * Output layout: M[g][o][i][j], g the row node, o = (dz+1)*9 + (dy+1)*3 + (dx+1)
+ * the offset of the column node g' = g + (dx, dy, dz) (periodic), i, j the
+ * tensor component; float[ncells][27][3][3].
+ *
+ *   grid       HOST int32[3], each >= 3 (so that the 27 offsets are distinct).
+ *   order      1.
+ *   precision  0 = TF32 tensor cores (tcgen05.mma kind::tf32, fp32 accumulate
+ *              in tensor memory); 1 = BF16 tensor cores (kind::f16); 2 = fp32
+ *              CUDA cores (no tensor cores; the A/B baseline).
+ *   n          number of particles.
+ *   pos        HOST array of 3 device float[n]; w device float[n] (q^2/m);
+ *   omega      HOST array of 3 device float[n] (omega = beta_s B(x_p) / c).
+ *   cell_offsets  device uint32[ncells + 1] from pcg_tile_sort with tile = 1:
+ *              the particles listed under cell c are [cell_offsets[c],
+ *              cell_offsets[c+1]).  A particle whose position is not inside the
+ *              cell it is listed under is still deposited correctly (through
+ *              global atomics) and flagged with PCG_FLAG_CELL_MISMATCH.
+ *   M          device float[ncells * 243], output (overwritten).
+ *   stats      device pcg_stats or NULL.
+ *   workspace  pcg_assemble_mass_matrix_workspace_size() bytes (currently 0).
+ */
+PCG_API pcg_status pcg_assemble_mass_matrix_workspace_size(const int32_t *grid, int64_t n, size_t *bytes);
+PCG_API pcg_status pcg_assemble_mass_matrix(const int32_t *grid, int32_t order, int32_t precision,
+                                    int64_t n, const float *const *pos, const float *w,
+                                    const float *const *omega, const uint32_t *cell_offsets,
+                                    float *M, pcg_stats *stats, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PCG_H */

@@ -1,0 +1,81 @@
+"""GPU parity of the 1D windowed CIC histogram against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import read_golden
+from helpers import DEPOSIT_TOL, dev, host, need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(pcg, x0, v, target, nsteps, dt, hw):
+    H, loss = pcg.deposit_cic1d(dev(x0), dev(v), dev(target), nsteps=nsteps, dt=dt, halfwidth=hw)
+    return host(H), float(host(loss)[0])
+
+
+def _check(H, L, x0, v, target, nsteps, dt, hw):
+    Hr, Lr, _ = oracle.cic1d(x0, v, target, target.size, nsteps, dt, hw)
+    scale = max(np.abs(Hr).max(), 1e-30)
+    assert np.abs(H - Hr).max() <= DEPOSIT_TOL * scale
+    # the loss is accumulated in fp64 from the fp32 histogram: its error is
+    # bounded by sum 2|H - t| |dH|, far below 1e-6 relative here
+    assert abs(L - Lr) <= 1e-6 * max(abs(Lr), 1.0)
+
+
+def test_workload_full_size():
+    pcg = need_gpu()
+    d = synth.cic1d()
+    H, L = _run(pcg, d["x0"], d["v"], d["target"], d["nsteps"], d["dt"], d["halfwidth"])
+    _check(H, L, d["x0"], d["v"], d["target"], d["nsteps"], d["dt"], d["halfwidth"])
+    assert (H > 0).sum() > 100
+
+
+def test_worked_example():
+    pcg = need_gpu()
+    rows = {r[0]: r[1:] for r in read_golden("cic1d_worked.txt")}
+    f = lambda k: np.array([float(x) for x in rows[k]], np.float32)
+    H, L = _run(pcg, f("x0"), f("v"), f("target"), int(rows["nsteps"][0]), float(rows["dt"][0]),
+                float(rows["halfwidth"][0]))
+    want = np.array([float(x) for x in rows["H_num"]]) / float(rows["H_den"][0])
+    assert np.allclose(H, want, rtol=0, atol=1e-6)
+    assert abs(L - float(rows["loss_num"][0]) / float(rows["loss_den"][0])) < 1e-6
+
+
+@pytest.mark.parametrize("n,nb,T,hw", [(1, 1024, 50, 0.005), (7, 4, 3, 0.3), (5000, 16384, 20, 0.01),
+                                       (3000, 1000, 9, 0.6), (40000, 512, 50, 0.002)])
+def test_sizes_and_windows(n, nb, T, hw):
+    pcg = need_gpu()
+    rng = np.random.default_rng(n + nb)
+    x0 = rng.random(n).astype(np.float32)
+    v = rng.normal(0, 0.3, n).astype(np.float32)
+    target = rng.random(nb).astype(np.float32)
+    H, L = _run(pcg, x0, v, target, T, 0.013, hw)
+    _check(H, L, x0, v, target, T, 0.013, hw)
+
+
+def test_positions_outside_unit_interval_wrap():
+    pcg = need_gpu()
+    rng = np.random.default_rng(5)
+    x0 = rng.uniform(-30, 30, 4000).astype(np.float32)
+    v = rng.normal(0, 2.0, 4000).astype(np.float32)
+    target = np.zeros(256, np.float32)
+    H, L = _run(pcg, x0, v, target, 40, 0.01, 0.01)
+    _check(H, L, x0, v, target, 40, 0.01, 0.01)
+
+
+def test_empty_input():
+    pcg = need_gpu()
+    target = np.linspace(0, 1, 64).astype(np.float32)
+    H, L = _run(pcg, np.zeros(0, np.float32), np.zeros(0, np.float32), target, 10, 0.01, 0.005)
+    assert np.all(H == 0)
+    assert abs(L - float(np.sum(target.astype(np.float64) ** 2))) < 1e-9
+
+
+def test_repeat_calls_overwrite():
+    pcg = need_gpu()
+    d = synth.cic1d(n=500, seed=7)
+    a = _run(pcg, d["x0"], d["v"], d["target"], 50, 0.01, 0.005)
+    b = _run(pcg, d["x0"], d["v"], d["target"], 50, 0.01, 0.005)
+    assert np.abs(a[0] - b[0]).max() <= 1e-6 * max(np.abs(a[0]).max(), 1e-30)
