@@ -1,0 +1,496 @@
+#!/usr/bin/env python
+"""Benchmark of the particle-to-grid deposit hot path on GB300.
+
+Headline workload (one "step" = the whole current-deposit path on one batch):
+  3D first-order (CIC) current deposit, periodic 256^3 grid, 16 particles per
+  cell (268,435,456 particles), sort-time positions x_s, deposit positions
+  x = x_s + v (0.1 % displaced by up to 3 cells), 8^3 tiles, 2-cell halo.
+  step = tile counting sort (key, count, scan, permute) + tiled deposit
+  (scratch tile, escape valve, flush).  Inputs stay resident in HBM; they are
+  far larger than L2 (7.5 GB vs 129 MB), so no L2 flush is needed between steps.
+
+Also measured in the same run (the other rows of the hot path, each on its own
+workload): the 1D windowed CIC histogram, the 2D CIC deposit on 512^2, the 3D
+quadratic deposit on the 192^3 density bump, and the ECSIM mass matrix on 64^3
+(TF32 and BF16 tensor cores, and the CUDA-core baseline).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "particle deposits/sec (M/s) and achieved HBM GB/s vs peak on 1 GB300"
+UNIT = "M deposits/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
+
+
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, keyed by kernel name.
+
+    Each line: <kernel> <bytes_per_launch> <units_per_launch> <source-hash>.  An
+    entry counts only while the kernel sources still hash to the recorded value.
+    """
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    out = {}
+    if not os.path.exists(p):
+        return out
+    cur = source_hash()
+    with open(p) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if len(line) == 4 and line[3] == cur:
+                out[line[0]] = (float(line[1]), float(line[2]))
+    return out
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "particle_cell_grid_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:12]
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={CLOCK_QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(", ") for r in self.file.read().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summarize(rows):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        busy = [r for r in rows if len(r) >= 10 and r[9].strip().isdigit() and int(r[9]) > 0] or rows
+        for r in busy:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for k, nm in enumerate(names):
+                if len(r) > 5 + k and "Active" in r[5 + k] and "Not" not in r[5 + k]:
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            self.dist = dist
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            self.dist.init_process_group(backend=backend)
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x):
+        if self.world == 1:
+            return x
+        import torch
+        dev = "cuda" if self.dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+def time_steps(step, steps, warmup, dist, stream, pcg=None):
+    """W untimed warm-up steps, then K steps between CUDA events on `stream`.
+
+    With `pcg` given, the library's per-kernel event timing is on for exactly
+    the K timed steps."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    if pcg is not None:
+        pcg.profile_collect()   # drop anything recorded before
+        pcg.profile_enable(True)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    if pcg is not None:
+        pcg.profile_enable(False)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)  # ms
+
+
+def roofline_entry(name, prof, bytes_per_launch, peak, traffic, units_per_launch):
+    launches, total_ms = prof[name]
+    avg_ms = total_ms / launches
+    gbs = bytes_per_launch / (avg_ms * 1e-3) / 1e9
+    tr = None
+    if name in traffic:
+        t_bytes, t_units = traffic[name]
+        tr = t_bytes * (units_per_launch / t_units)  # scaled to a full launch when captured smaller
+    return {"bound": "hbm", "kernel": name, "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "traffic": None if tr is None else round(tr),
+            "algorithmic_bytes": int(bytes_per_launch), "avg_ms": round(avg_ms, 4), "launches": launches}
+
+
+def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
+    """Time sort + tiled deposit on a current-deposit workload; returns a dict."""
+    import torch
+    grid, dim = d["grid"], len(d["grid"])
+    n = d["n"]
+    stream = torch.cuda.current_stream()
+    dev = lambda a: torch.from_numpy(a).cuda()
+    pos = [dev(p) for p in d["pos"]]
+    vel = [dev(v) for v in d["vel"]]
+    q = dev(d["q"])
+    separate_keys = d["key_pos"] is not d["pos"]
+    kp = [dev(k) for k in d["key_pos"]] if separate_keys else pos
+    payload = pos + vel + [q]
+    out = [torch.empty_like(p) for p in payload]
+    nt = pcg.n_tiles(grid, d["tile"])
+    offs = torch.empty(nt + 1, dtype=torch.int32, device="cuda")
+    J = torch.empty((3,) + tuple(reversed(grid)), dtype=torch.float32, device="cuda")
+    ws_s = torch.empty(max(pcg.tile_sort_workspace_size(grid, d["tile"], n), 256), dtype=torch.uint8, device="cuda")
+    ws_d = torch.empty(max(pcg.deposit_current_workspace_size(grid, d["tile"], n), 256), dtype=torch.uint8,
+                       device="cuda")
+    stats = pcg.new_stats()
+
+    def step():
+        pcg.tile_sort(grid, d["tile"], kp, payload, out=out, tile_offsets=offs, workspace=ws_s)
+        pcg.deposit_current(grid, d["order"], out[:dim], out[dim:dim + 3], out[dim + 3], tile_offsets=offs,
+                            tile=d["tile"], halo=d["halo"], J=J, stats=stats, workspace=ws_d)
+
+    step()
+    torch.cuda.synchronize()
+    st = pcg.read_stats(stats)
+    ms = time_steps(step, steps, warmup, dist, stream, pcg=pcg)
+    timed = pcg.profile_collect()
+    ms = dist.max(ms)
+    res = {"n": n, "ms_per_step": ms / steps, "value": n * steps * dist.world / (ms * 1e-3) / 1e6,
+           "escaped_per_step": st["n_escaped"], "invalid": st["n_invalid"], "profile": timed}
+    # algorithmic bytes per launch of the main kernels
+    kbytes = 4 * dim * (1 if separate_keys else 0)
+    node_bytes = 12 * int(np.prod(grid))
+    alg = {
+        "deposit_tiled": n * (4 * (dim + 4)) + node_bytes,
+        "sort_scatter": n * (kbytes + 2 * 4 * (dim + 4)),
+        "sort_count": n * 4 * dim,
+    }
+    kern = {}
+    for name, b in alg.items():
+        if name in timed:
+            kern[name] = roofline_entry(name, timed, b, peaks["hbm_gbs"], traffic, n)
+    res["kernels"] = kern
+    dom = max(timed.items(), key=lambda kv: kv[1][1])[0]
+    res["dominant"] = dom
+    res["gpu_launches"] = sum(v[0] for v in timed.values())
+
+    if e2e_steps:
+        # end to end through the public API: pinned host inputs -> device, the
+        # step, device -> host read of J, every step
+        h_in = [torch.from_numpy(a).pin_memory() for a in (list(d["key_pos"]) if separate_keys else [])
+                + list(d["pos"]) + list(d["vel"]) + [d["q"]]]
+        d_in = (kp if separate_keys else []) + payload
+        h_J = torch.empty(J.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            for h, t in zip(h_in, d_in):
+                t.copy_(h, non_blocking=True)
+            step()
+            h_J.copy_(J, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        ms_e = time_steps(e2e_step, e2e_steps, 1, dist, stream)
+        ms_e = dist.max(ms_e)
+        res["e2e"] = {"value": round(n * e2e_steps * dist.world / (ms_e * 1e-3) / 1e6, 3), "unit": UNIT,
+                      "h2d_bytes_per_step": int(sum(h.numel() * 4 for h in h_in)),
+                      "d2h_bytes_per_step": int(J.numel() * 4), "ms_per_step": round(ms_e / e2e_steps, 3)}
+        del h_in, h_J
+    del pos, vel, q, kp, payload, out, J, ws_s, ws_d
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_current(d, budget_s=12.0):
+    """The fp64 oracle as it stands, single-threaded, on a bounded random sample."""
+    import oracle
+    n = d["n"]
+    s0 = min(n, 500_000)
+    t = time.perf_counter()
+    oracle.deposit_current(d["grid"], d["order"], [p[:s0] for p in d["pos"]], [v[:s0] for v in d["vel"]],
+                           d["q"][:s0])
+    t0 = time.perf_counter() - t
+    s = int(min(n, max(s0, s0 * budget_s / max(t0, 1e-3))))
+    t = time.perf_counter()
+    oracle.deposit_current(d["grid"], d["order"], [p[:s] for p in d["pos"]], [v[:s] for v in d["vel"]],
+                           d["q"][:s])
+    dt = time.perf_counter() - t
+    return {"value": round(s / dt / 1e6, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {s} of {n} particles (random order) of the same workload, full grid, "
+                      f"fp64 C oracle single thread, {dt:.1f} s"}
+
+
+def mass_workload(pcg, steps, warmup, dist, peaks, traffic):
+    import torch
+    import synth
+    d = synth.mass3d()
+    grid, n = d["grid"], d["n"]
+    dev = lambda a: torch.from_numpy(a).cuda()
+    dp = [dev(p) for p in d["pos"]]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(d["w"])] + [dev(o) for o in d["omega"]])
+    M = torch.empty(tuple(reversed(grid)) + (27, 3, 3), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    res = {"workload": "mass3d 64^3 x 64 ppc (CIC, 27 offsets x 3x3 blocks)", "particles": n}
+    alg_bytes = n * 28 + M.numel() * 4
+    useful_flops = n * 8 * 8 * 9 * 2
+    issued = {"tf32": n * 128 * 16 * 2, "bf16": n * 128 * 16 * 2, "simt": 0}
+    tf32_peak = peaks["bf16_tflops"] / 2.0   # dense TF32 = half the bf16 rate (nominal 1.1 vs 2.25 PF)
+    for prec in ("tf32", "bf16", "simt"):
+        step = lambda: pcg.assemble_mass_matrix(grid, out[:3], out[3], out[4:7], offs, precision=prec, M=M)
+        step()
+        ms = time_steps(step, steps, warmup, dist, stream, pcg=pcg)
+        timed = pcg.profile_collect()
+        name = f"mass_matrix_{prec}"
+        ent = roofline_entry(name, timed, alg_bytes, peaks["hbm_gbs"], traffic, n)
+        kms = ent["avg_ms"]
+        r = {"ms_per_call": round(ms / steps, 4), "kernel_ms": kms,
+             "M_particles_per_s": round(n / (ms / steps * 1e-3) / 1e6, 1), "roofline": ent,
+             "useful_tflops": round(useful_flops / (kms * 1e-3) / 1e12, 2)}
+        if prec != "simt":
+            pk = tf32_peak if prec == "tf32" else peaks["bf16_tflops"]
+            r["issued_tflops"] = round(issued[prec] / (kms * 1e-3) / 1e12, 2)
+            r["tensor_frac_issued"] = round(issued[prec] / (kms * 1e-3) / 1e12 / pk, 4)
+            r["tensor_peak_tflops"] = pk
+        res[prec] = r
+    del dp, out, offs, M
+    torch.cuda.empty_cache()
+    return res
+
+
+def cic1d_workload(pcg, steps, warmup, dist):
+    import torch
+    import synth
+    d = synth.cic1d()
+    dev = lambda a: torch.from_numpy(a).cuda()
+    x0, v, tg = dev(d["x0"]), dev(d["v"]), dev(d["target"])
+    H = torch.empty(d["nbins"], dtype=torch.float32, device="cuda")
+    L = torch.empty(1, dtype=torch.float64, device="cuda")
+    step = lambda: pcg.deposit_cic1d(x0, v, tg, d["nsteps"], d["dt"], d["halfwidth"], H=H, loss=L)
+    ms = time_steps(step, steps, warmup, dist, torch.cuda.current_stream())
+    us = ms * 1e3 / steps
+    return {"workload": "cic1d N=2000, 1024 bins, T=50", "us_per_call": round(us, 2),
+            "M_particle_steps_per_s": round(2000 * 50 / (us * 1e-6) / 1e6, 1),
+            "note": "latency-bound (16 KB in, 4 KB out): one cluster launch per call, no roofline fraction"}
+
+
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import particle_cell_grid_gb300 as pcg
+    import synth
+
+    dist = Dist(args.gpus)
+    dist.init("nccl")
+    torch.cuda.set_device(dist.local)
+    pcg._lib.load()  # fails loudly without the library
+    peaks, peak_src = load_peaks()
+    traffic = load_traffic()
+
+    g = args.grid
+    d = synth.cic3d_drift(grid=(g, g, g))
+    sampler = ClockSampler(dist.local)
+    sampler.start()
+    main = current_workload(pcg, d, args.steps, args.warmup, dist, peaks, traffic, e2e_steps=args.e2e_steps)
+    clocks = ClockSampler.summarize(sampler.stop())
+    cpu = cpu_baseline_current(d) if (dist.rank == 0 and dist.world == 1 and not args.no_cpu) else None
+    del d
+
+    dom = main["dominant"]
+    roof = main["kernels"].get(dom) or next(iter(main["kernels"].values()))
+    line = {
+        "metric": METRIC, "value": round(main["value"], 3), "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(main["ms_per_step"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded numpy PCG64; recipe in DESIGN.md)",
+        "config": {"workload": f"cic3d_drift {g}^3 x 16 ppc, CIC current deposit (sort + tiled deposit)",
+                   "grid": [g, g, g], "particles": main["n"], "order": 1, "tile": 8, "halo": 2,
+                   "step": "pcg_tile_sort + pcg_deposit_current", "parallelism": "replicas" if dist.world > 1 else "1 GPU",
+                   "l2": "inputs (7.5 GB) larger than L2 (129 MB); no flush"},
+        "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")} |
+                    {"kernel": roof["kernel"], "peak_source": f"{peak_src} hbm_gbs (copy, burst)"},
+        "kernels": main["kernels"],
+        "profile_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in main["profile"].items()},
+        "escaped_per_step": main["escaped_per_step"],
+        "gpu_launches": main["gpu_launches"],
+        "clocks": clocks,
+    }
+    if "e2e" in main:
+        line["e2e"] = main["e2e"]
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if dist.world == 1 and not args.main_only:
+        wl = {}
+        ks, kw = max(3, args.steps // 10), max(3, args.warmup)
+        wl["cic1d"] = cic1d_workload(pcg, 200, 10, dist)
+        d2 = synth.cic2d()
+        r2 = current_workload(pcg, d2, max(20, args.steps // 2), kw, dist, peaks, traffic)
+        wl["cic2d_512"] = {"workload": "cic2d 512^2 x 8 ppc", "value": round(r2["value"], 1), "unit": UNIT,
+                           "ms_per_step": round(r2["ms_per_step"], 4), "kernels": r2["kernels"]}
+        del d2
+        d4 = synth.quad3d_bump()
+        r4 = current_workload(pcg, d4, ks, kw, dist, peaks, traffic)
+        wl["quad3d_bump_192"] = {"workload": "quad3d_bump 192^3, mean 32 ppc, peak 320", "particles": r4["n"],
+                                 "value": round(r4["value"], 1), "unit": UNIT,
+                                 "ms_per_step": round(r4["ms_per_step"], 4), "kernels": r4["kernels"],
+                                 "escaped_per_step": r4["escaped_per_step"]}
+        del d4
+        wl["mass3d_64"] = mass_workload(pcg, ks, kw, dist, peaks, traffic)
+        line["workloads"] = wl
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def run_reference(args):
+    """The oracle as it stands on the host cores, on bounded samples of the same workload."""
+    dist = Dist(args.gpus)
+    if dist.rank != 0:
+        return
+    import oracle
+    import synth
+    d = synth.cic3d_drift()
+    n = d["n"]
+    total = args.steps + args.warmup
+    s0 = 200_000
+    t = time.perf_counter()
+    oracle.deposit_current(d["grid"], 1, [p[:s0] for p in d["pos"]], [v[:s0] for v in d["vel"]], d["q"][:s0])
+    rate = s0 / (time.perf_counter() - t)
+    budget = 90.0  # seconds for the whole --steps/--warmup run
+    s = int(max(20_000, min(n, rate * budget / total)))
+    take = lambda k: ([p[k * s % n:k * s % n + s] for p in d["pos"]], [v[k * s % n:k * s % n + s] for v in d["vel"]],
+                      d["q"][k * s % n:k * s % n + s])
+    for k in range(args.warmup):
+        oracle.deposit_current(d["grid"], 1, *take(k))
+    t = time.perf_counter()
+    for k in range(args.steps):
+        oracle.deposit_current(d["grid"], 1, *take(args.warmup + k))
+    dt = time.perf_counter() - t
+    value = s * args.steps / dt / 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy PCG64)",
+            "config": {"workload": "cic3d_drift 256^3 x 16 ppc, CIC current deposit", "grid": [256, 256, 256],
+                       "particles": n, "sample_per_step": s},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{s} consecutive particles per step of the {n}-particle workload "
+                                       f"(random order), fp64 C oracle, single thread"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--grid", type=int, default=256, help="edge of the headline workload's grid (256 = full size)")
+    ap.add_argument("--main-only", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -224,6 +224,22 @@ PCG_API pcg_status pcg_assemble_mass_matrix(const int32_t *grid, int32_t order, 
                                     float *M, pcg_stats *stats, void *workspace,
                                     size_t workspace_bytes, void *stream);
 
+/* -------------------------------------------------------------------------
+ * Kernel timing (tracing aid; no counterpart in the method).
+ * While enabled, every kernel the library launches is bracketed by two CUDA
+ * events recorded on its launch stream.  pcg_profile_collect() waits for the
+ * recorded events, aggregates them by kernel name and forgets them:
+ *   names     HOST char[max_entries][64], NUL-terminated kernel names;
+ *   launches  HOST int64[max_entries], total_ms HOST double[max_entries];
+ *   n_entries HOST int32: number of distinct kernels seen (may exceed
+ *             max_entries; only the first max_entries are written).
+ * Returns PCG_ERR_CUDA if some event could not be timed.  Thread-safe; the
+ * state is process-wide.  Recording costs two event records per launch.
+ */
+PCG_API pcg_status pcg_profile_enable(int32_t enable);
+PCG_API pcg_status pcg_profile_collect(int32_t max_entries, char *names, int64_t *launches,
+                                       double *total_ms, int32_t *n_entries);
+
 #ifdef __cplusplus
 }
 #endif

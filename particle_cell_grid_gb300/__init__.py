@@ -23,6 +23,7 @@ __all__ = [
     "PcgError", "version", "deposit_cic1d", "tile_sort", "tile_sort_workspace_size",
     "deposit_current", "deposit_current_workspace_size", "assemble_mass_matrix",
     "assemble_mass_matrix_workspace_size", "new_stats", "read_stats", "n_tiles",
+    "profile_enable", "profile_collect",
 ]
 
 STATS_BYTES = 24
@@ -215,3 +216,24 @@ def assemble_mass_matrix(grid, pos, w, omega, cell_offsets, precision="tf32", M=
                                               _ptr(ws), _ws_bytes(ws), _stream(stream))
     check(st, "pcg_assemble_mass_matrix")
     return M
+
+
+# ---------------------------------------------------------------------------
+def profile_enable(on: bool = True) -> None:
+    """Start / stop recording an event pair around every library kernel launch."""
+    check(_lib.load().pcg_profile_enable(1 if on else 0), "pcg_profile_enable")
+
+
+def profile_collect(max_entries: int = 64) -> dict:
+    """{kernel name: (launches, total ms)} for the launches recorded so far (then cleared)."""
+    names = ctypes.create_string_buffer(64 * max_entries)
+    launches = (ctypes.c_int64 * max_entries)()
+    total = (ctypes.c_double * max_entries)()
+    count = ctypes.c_int32(0)
+    check(_lib.load().pcg_profile_collect(max_entries, names, launches, total, ctypes.byref(count)),
+          "pcg_profile_collect")
+    out = {}
+    for i in range(min(count.value, max_entries)):
+        nm = names.raw[64 * i:64 * (i + 1)].split(b"\0", 1)[0].decode()
+        out[nm] = (int(launches[i]), float(total[i]))
+    return out

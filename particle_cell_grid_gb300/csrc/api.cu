@@ -24,6 +24,7 @@ pcg_status zero_f32(float *p, size_t count, cudaStream_t s) {
     size_t cap = (size_t)kNumSMs * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    prof::Mark mk("zero_f32", s);
     zero_f32_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, count);
     return launch_status();
 }

@@ -133,6 +133,7 @@ extern "C" pcg_status pcg_deposit_cic1d(const float *x0, const float *v, int64_t
     if (smem > 48 * 1024)
         PCG_CHECK_CUDA(cudaFuncSetAttribute(cic1d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             (int)smem));
+    prof::Mark mk("cic1d", as_stream(stream));
     cic1d_kernel<<<kCtas, kThreads, smem, as_stream(stream)>>>(x0, v, (long long)n, target, nbins,
                                                               nsteps, dt, halfwidth, H, loss);
     return launch_status();

@@ -144,6 +144,7 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
         const size_t cap = (size_t)kNumSMs * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
+        prof::Mark mk("deposit_prep", s);
         prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(J, nJ, tiled ? tile_offsets : nullptr,
                                                     g.n_tiles, n, chunk, chunk_tile, nchunks,
                                                     ctr.flags);
@@ -154,6 +155,7 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
         const long long want = (n + 255) / 256;
         const long long cap = (long long)kNumSMs * 16;
         const unsigned blocks = (unsigned)(want < cap ? want : cap);
+        prof::Mark mk("deposit_flat", s);
         if (dim == 2) {
             if (order == 1) deposit_flat_kernel<2, 1><<<blocks, 256, 0, s>>>(g, P, n, J, ctr);
             else deposit_flat_kernel<2, 2><<<blocks, 256, 0, s>>>(g, P, n, J, ctr);

@@ -103,12 +103,15 @@ __device__ __forceinline__ void deposit_global(const Geom &g, float *__restrict_
     }
 }
 
-// Local coordinate of a first node relative to the tile origin, periodic minimum image.
+// Tile-local coordinate of a stencil's first node (S nodes per axis) relative to
+// the tile origin, taken periodically: the non-negative offset when the stencil
+// then ends inside the scratch window [-HALO, TILE + HALO), else the offset one
+// period below (a particle that drifted across the lower periodic boundary).
+template <int S, int TILE, int HALO>
 __device__ __forceinline__ int local_index(int f, int origin, int N) {
-    int d = f - origin;
-    if (2 * d >= N) d -= N;
-    else if (2 * d < -N) d += N;
-    return d;
+    int d = (f - origin) % N;
+    if (d < 0) d += N;
+    return d + S - 1 < TILE + HALO ? d : d - N;
 }
 
 }  // namespace dep

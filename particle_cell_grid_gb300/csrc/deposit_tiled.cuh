@@ -35,9 +35,9 @@ __device__ __forceinline__ void deposit_one(const Geom &g, float *__restrict__ s
     int fz = 0;
     if (DIM == 3) fz = axis_weights<ORDER>(z, wz);
     else wz[0] = 1.f;
-    const int lx = local_index(fx, ox, g.N[0]);
-    const int ly = local_index(fy, oy, g.N[1]);
-    const int lz = DIM == 3 ? local_index(fz, oz, g.N[2]) : 0;
+    const int lx = local_index<S, TILE, HALO>(fx, ox, g.N[0]);
+    const int ly = local_index<S, TILE, HALO>(fy, oy, g.N[1]);
+    const int lz = DIM == 3 ? local_index<S, TILE, HALO>(fz, oz, g.N[2]) : 0;
     // fit test: every stencil node inside [-HALO, TILE + HALO) on every axis
     bool fits = (lx >= -HALO) & (lx + S - 1 < TILE + HALO) & (ly >= -HALO) &
                 (ly + S - 1 < TILE + HALO);
@@ -182,6 +182,7 @@ pcg_status launch_tiled(const Geom &g, long long n, const Particles &P, const ui
     if (nchunks == 0) return PCG_OK;
     const bool vec4 = aligned16(P.x) && aligned16(P.y) && (DIM == 2 || aligned16(P.z)) &&
                       aligned16(P.vx) && aligned16(P.vy) && aligned16(P.vz) && aligned16(P.q);
+    prof::Mark mk("deposit_tiled", s);
     deposit_tiled_kernel<DIM, ORDER, TILE, HALO>
         <<<(unsigned)nchunks, block, 0, s>>>(g, P, n, offs, chunk_tile, chunk, J, ctr, vec4);
     return launch_status();

@@ -459,6 +459,7 @@ pcg_status launch(const Args &A, cudaStream_t s) {
                                         (int)smem));
     const long long nblocks = (long long)A.nb[0] * A.nb[1] * A.nb[2];
     const long long grid = nblocks < kNumSMs ? nblocks : kNumSMs;
+    prof::Mark mk(MODE == TF32 ? "mass_matrix_tf32" : MODE == BF16 ? "mass_matrix_bf16" : "mass_matrix_simt", s);
     mass_kernel<MODE><<<(unsigned)grid, kThreads, smem, s>>>(A);
     return launch_status();
 }

@@ -261,13 +261,23 @@ pcg_status run_sort(const TileGrid &tg, const Plan &pl, long long n, const float
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                 (int)pl.smem));
         }
-        count_chunked_kernel<DIM, TILE><<<pl.G, kSortThreads, pl.smem, s>>>(
-            g, kp[0], kp[1], kz, n, pl.chunk, counts, pl.B, n_invalid);
+        {
+            prof::Mark mk("sort_count", s);
+            count_chunked_kernel<DIM, TILE><<<pl.G, kSortThreads, pl.smem, s>>>(
+                g, kp[0], kp[1], kz, n, pl.chunk, counts, pl.B, n_invalid);
+        }
         PCG_CHECK_LAUNCH();
-        colscan_kernel<<<(pl.B + 255) / 256, 256, 0, s>>>(counts, totals, pl.G, pl.B);
+        {
+            prof::Mark mk("sort_colscan", s);
+            colscan_kernel<<<(pl.B + 255) / 256, 256, 0, s>>>(counts, totals, pl.G, pl.B);
+        }
         PCG_CHECK_LAUNCH();
-        scan_one_cta_kernel<<<1, 1024, 0, s>>>(totals, offs, nullptr, pl.B);
+        {
+            prof::Mark mk("sort_scan", s);
+            scan_one_cta_kernel<<<1, 1024, 0, s>>>(totals, offs, nullptr, pl.B);
+        }
         PCG_CHECK_LAUNCH();
+        prof::Mark mk("sort_scatter", s);
         scatter_chunked_kernel<DIM, TILE><<<pl.G, kSortThreads, pl.smem, s>>>(
             g, kp[0], kp[1], kz, n, pl.chunk, counts, offs, pl.B, py, np);
         return launch_status();
@@ -278,10 +288,17 @@ pcg_status run_sort(const TileGrid &tg, const Plan &pl, long long n, const float
     pcg_status st = zero_f32(reinterpret_cast<float *>(totals), pl.B, s);
     if (st != PCG_OK) return st;
     const unsigned grid = (unsigned)kNumSMs * 8;
-    count_global_kernel<DIM, TILE><<<grid, 256, 0, s>>>(g, kp[0], kp[1], kz, n, totals, n_invalid);
+    {
+        prof::Mark mk("sort_count_global", s);
+        count_global_kernel<DIM, TILE><<<grid, 256, 0, s>>>(g, kp[0], kp[1], kz, n, totals, n_invalid);
+    }
     PCG_CHECK_LAUNCH();
-    scan_one_cta_kernel<<<1, 1024, 0, s>>>(totals, offs, cursor, pl.B);
+    {
+        prof::Mark mk("sort_scan", s);
+        scan_one_cta_kernel<<<1, 1024, 0, s>>>(totals, offs, cursor, pl.B);
+    }
     PCG_CHECK_LAUNCH();
+    prof::Mark mk("sort_scatter_global", s);
     scatter_global_kernel<DIM, TILE><<<grid, 256, 0, s>>>(g, kp[0], kp[1], kz, n, cursor, py, np);
     return launch_status();
 }
