@@ -84,7 +84,9 @@ def test_cic3d_256_drift():
     d = synth.cic3d_drift()
     J, st = _run_current(pcg, d)
     assert st["n_invalid"] == 0
-    assert st["n_escaped"] >= 0.5 * d["displaced"].size  # displaced particles leave the halo
+    # a displacement U[-3, 3] per axis leaves the 2-cell halo with probability
+    # 5/96 per axis for a uniform in-tile position (~15 % over three axes)
+    assert 0.10 * d["displaced"].size <= st["n_escaped"] <= 0.25 * d["displaced"].size
     _check_totals(d, J)
     _check_boxes(d, J, [((0, 0, 0), (12, 12, 12)), ((120, 64, 250), (136, 80, 262)),
                         ((200, 7, 99), (213, 21, 110))])
