@@ -186,6 +186,34 @@ PCG_API pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int32_t
                                void *workspace, size_t workspace_bytes, void *stream);
 
 /* -------------------------------------------------------------------------
+ * pcg_deposit_current without a workspace: for callers that cannot allocate
+ * device memory (a host callback, a plugin that is handed only its input and
+ * output buffers, an application whose memory pool forbids run-time
+ * allocation).  The pages have no counterpart: this is a packaging variant of
+ * pcg_deposit_current, which it calls with its own scratch.
+ *
+ * Arguments, outputs, stats and errors are those of pcg_deposit_current minus
+ * the workspace.  The tiled path's scratch (one 32-bit entry per chunk of up
+ * to 16384 particles) is a fixed 256 KB device array inside the library, held
+ * on every GPU that loads it until the process exits; so this entry point
+ * accepts at most 65536 chunks, i.e. n <= 2^30 particles when tile_offsets is
+ * given, and returns PCG_ERR_WORKSPACE above that (before launching anything).
+ * The flat path (tile_offsets NULL) uses no scratch and has no such limit.
+ *
+ * It allocates nothing.  The first call made on a device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Every call shares the one array and
+ * each call rewrites every entry it reads, so nothing needs clearing between
+ * calls; but calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on the array and must not be issued.
+ */
+PCG_API pcg_status pcg_deposit_current_noalloc(int32_t dim, const int32_t *grid, int32_t order,
+                                               int32_t tile, int32_t halo, int32_t block, int64_t n,
+                                               const float *const *pos, const float *const *vel,
+                                               const float *q, const uint32_t *tile_offsets, float *J,
+                                               pcg_stats *stats, void *stream);
+
+/* -------------------------------------------------------------------------
  * ECSIM block mass matrix with first-order (CIC) B-splines.
  * Defined by Pennati & Markidis, Sec. 2.1, Eqs. (4)-(6):
  *   M^{ij}_{g g'} = sum_p s_p^{ij} W_pg W_pg',  s_p = w_p alpha_p,

@@ -1,6 +1,8 @@
 // deposit.cu -- C ABI of the current deposit: argument checks, J zeroing, the
 // chunk-to-tile map, the flat (all-global-reduction) kernel and the tiled
 // dispatch.  See deposit.cuh for the method and its sources.
+#include <mutex>
+
 #include "deposit.cuh"
 
 namespace pcg {
@@ -170,4 +172,73 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
                                        chunk, threads, s)
                     : deposit_tiled_3d(order, tile, halo, g, n, P, tile_offsets, J, ctr, chunk_tile,
                                        chunk, threads, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of pcg_deposit_current.
+//
+// Some callers cannot allocate device memory at all: code running inside a
+// host callback or a custom allocator, plugins handed only their input and
+// output buffers by a host application, or a pool that forbids cudaMalloc at
+// run time.  This entry point takes exactly the arguments of
+// pcg_deposit_current except the workspace: the only scratch the tiled path
+// needs, the chunk-to-tile map (one 32-bit entry per chunk of particles), lives
+// in the fixed device array below, which every GPU that loads the library holds
+// until the process exits.
+//
+// Host code must not pass the array's name to a kernel: on the host it is only
+// a stand-in for the symbol.  Its device address is looked up once per device,
+// with that device current, by the first call made on that device.
+namespace pcg {
+namespace {
+
+constexpr size_t kNoAllocChunks = 65536;  // 256 KB: up to 65536 chunks of <= 16384 particles
+static __device__ __align__(256) unsigned g_chunk_tile[kNoAllocChunks];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned *g_chunk_tile_addr[kMaxDevices] = {};
+
+// Device address of g_chunk_tile on the current device (set up on first use).
+pcg_status noalloc_scratch(unsigned **out) {
+    int dev = 0;
+    PCG_CHECK_CUDA(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= kMaxDevices) return PCG_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_chunk_tile_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_chunk_tile) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return PCG_ERR_CUDA;
+        }
+        g_chunk_tile_addr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_chunk_tile_addr[dev];
+    return PCG_OK;
+}
+
+}  // namespace
+}  // namespace pcg
+
+extern "C" pcg_status pcg_deposit_current_noalloc(int32_t dim, const int32_t *grid, int32_t order,
+                                                  int32_t tile, int32_t halo, int32_t block,
+                                                  int64_t n, const float *const *pos,
+                                                  const float *const *vel, const float *q,
+                                                  const uint32_t *tile_offsets, float *J,
+                                                  pcg_stats *stats, void *stream) {
+    using namespace pcg;
+    if (n < 0 || n >= 0xffffffffll) return PCG_ERR_INVALID_ARG;
+    const long long chunk = chunk_for(n);
+    const long long nchunks = (n + chunk - 1) / chunk;
+    if (tile_offsets != nullptr && (size_t)nchunks > kNoAllocChunks) return PCG_ERR_WORKSPACE;
+    unsigned *scratch = nullptr;
+    if (tile_offsets != nullptr && n > 0) {
+        pcg_status st = noalloc_scratch(&scratch);
+        if (st != PCG_OK) return st;
+    }
+    // every entry the kernels read is written by this call's prep kernel first,
+    // so the array needs no clearing between calls
+    return pcg_deposit_current(dim, grid, order, tile, halo, block, n, pos, vel, q, tile_offsets, J,
+                               stats, scratch, scratch ? kNoAllocChunks * sizeof(unsigned) : 0,
+                               stream);
 }
