@@ -233,7 +233,8 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
     nt = pcg.n_tiles(grid, d["tile"])
     offs = torch.empty(nt + 1, dtype=torch.int32, device="cuda")
     J = torch.empty((3,) + tuple(reversed(grid)), dtype=torch.float32, device="cuda")
-    ws_s = torch.empty(max(pcg.tile_sort_workspace_size(grid, d["tile"], n), 256), dtype=torch.uint8, device="cuda")
+    ws_s = torch.empty(max(pcg.tile_sort_workspace_size(grid, d["tile"], n, len(payload)), 256), dtype=torch.uint8,
+                       device="cuda")
     ws_d = torch.empty(max(pcg.deposit_current_workspace_size(grid, d["tile"], n), 256), dtype=torch.uint8,
                        device="cuda")
     stats = pcg.new_stats()

@@ -131,12 +131,17 @@ PCG_API pcg_status pcg_deposit_cic1d(const float *x0, const float *v, int64_t n,
  *              [tile_offsets[t], tile_offsets[t+1]); invalid particles fill
  *              [tile_offsets[n_tiles], n).  Order inside a tile is unspecified.
  *   stats      device pcg_stats or NULL; n_invalid counts the sentinel bin.
- *   workspace  device memory of at least pcg_tile_sort_workspace_size() bytes,
- *              256-byte aligned; contents on entry are irrelevant.
- * Launches: 3 (bin count <= 32769, block-privatised counts) or 4 otherwise.
+ *   workspace  device memory of at least pcg_tile_sort_workspace_size() bytes
+ *              (same dim, grid, tile, n and n_payload), 256-byte aligned;
+ *              contents on entry are irrelevant.  When the permuted payload
+ *              does not fit in L2 the sort runs as two partition passes and the
+ *              workspace also holds the intermediate arrays, about
+ *              4 * (n_payload + 1) * n bytes.
+ * Launches: 4 while the output fits in L2 (count, column scan, scan,
+ * scatter), 6-7 otherwise (count, scan, bucket set-up, two partition passes).
  */
 PCG_API pcg_status pcg_tile_sort_workspace_size(int32_t dim, const int32_t *grid, int32_t tile, int64_t n,
-                                        size_t *bytes);
+                                        int32_t n_payload, size_t *bytes);
 PCG_API pcg_status pcg_tile_sort(int32_t dim, const int32_t *grid, int32_t tile, int64_t n,
                          const float *const *key_pos, int32_t n_payload,
                          const void *const *payload_in, void *const *payload_out,

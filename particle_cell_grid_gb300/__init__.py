@@ -114,9 +114,9 @@ def deposit_cic1d(x0, v, target, nsteps=50, dt=0.01, halfwidth=0.005, H=None, lo
 
 
 # ---------------------------------------------------------------------------
-def tile_sort_workspace_size(grid, tile, n) -> int:
+def tile_sort_workspace_size(grid, tile, n, n_payload=7) -> int:
     out = ctypes.c_size_t(0)
-    check(_lib.load().pcg_tile_sort_workspace_size(len(grid), _grid_arr(grid), int(tile), int(n),
+    check(_lib.load().pcg_tile_sort_workspace_size(len(grid), _grid_arr(grid), int(tile), int(n), int(n_payload),
                                                     ctypes.byref(out)), "pcg_tile_sort_workspace_size")
     return out.value
 
@@ -145,7 +145,7 @@ def tile_sort(grid, tile, key_pos, payload, out=None, tile_offsets=None, stats=N
         tile_offsets = torch.empty(nt + 1, dtype=torch.int32, device=dev)
     if tile_offsets.numel() != nt + 1 or tile_offsets.element_size() != 4:
         raise ValueError("tile_offsets must hold n_tiles + 1 32-bit entries")
-    ws = _workspace(tile_sort_workspace_size(grid, tile, n), dev, workspace)
+    ws = _workspace(tile_sort_workspace_size(grid, tile, n, len(payload)), dev, workspace)
     st = _lib.load().pcg_tile_sort(dim, _grid_arr(grid), int(tile), n, _ptr_arr(key_pos, 3),
                                    len(payload), _ptr_arr(payload), _ptr_arr(out), _ptr(tile_offsets),
                                    _ptr(stats), _ptr(ws), _ws_bytes(ws), _stream(stream))

@@ -199,41 +199,317 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Two-pass partition for outputs larger than L2 (MSD order).
+// Pass 1 moves every particle into one of <= 256 coarse buckets of `tpb`
+// consecutive tiles, pass 2 into its tile inside the bucket.  Each CTA takes a
+// batch of kBatch consecutive particles, counts their digits in shared memory,
+// reserves one contiguous global range per digit with a single global atomic,
+// reorders the batch in shared memory and writes each digit's run with
+// consecutive threads, so global writes leave the SM as contiguous runs and the
+// open (partly written) sectors are one per bucket or tile frontier.
+constexpr int kPartThreads = 512;
+constexpr int kBatch = 2048;
+constexpr int kItems = kBatch / kPartThreads;
+constexpr unsigned kMaxPassBins = 2048;
+constexpr unsigned kMaxBuckets = 256;
+
+// Exclusive scan of v[0..nb) in place (nb <= kMaxPassBins) by one CTA of
+// kPartThreads threads; returns nothing, v holds the exclusive prefix after.
+__device__ void block_exclusive_scan(unsigned *v, unsigned nb, unsigned *warp_tot) {
+    constexpr int PER = kMaxPassBins / kPartThreads;  // 4 bins per thread
+    const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned loc[PER];
+    unsigned sum = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const unsigned b = threadIdx.x * PER + i;
+        loc[i] = b < nb ? v[b] : 0u;
+        sum += loc[i];
+    }
+    unsigned incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= (unsigned)o) incl += t;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned w = lane < kPartThreads / 32 ? warp_tot[lane] : 0u;
+        unsigned wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= (unsigned)o) wi += t;
+        }
+        if (lane < kPartThreads / 32) warp_tot[lane] = wi - w;
+    }
+    __syncthreads();
+    unsigned run = warp_tot[warp] + incl - sum;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const unsigned b = threadIdx.x * PER + i;
+        if (b < nb) v[b] = run;
+        run += loc[i];
+    }
+    __syncthreads();
+}
+
+// PASS 1: digit = bucket of the tile key computed from key positions; writes the
+//         payload and the key to the intermediate arrays (or, with FINAL, the
+//         payload straight to the output when one pass suffices).
+// PASS 2: digit = tile inside the batch's bucket; key read from the
+//         intermediate arrays; writes the final payload.
+template <int DIM, int TILE, int PASS, bool FINAL>
+__global__ void __launch_bounds__(kPartThreads)
+    partition_kernel(KeyGeom g, const float *__restrict__ kx, const float *__restrict__ ky,
+                     const float *__restrict__ kz, long long n, Payload pl, int np,
+                     const unsigned *__restrict__ in_key, unsigned *__restrict__ out_key,
+                     unsigned *__restrict__ gcursor, unsigned tpb, unsigned B,
+                     const unsigned *__restrict__ batch_off, const uint32_t *__restrict__ offs,
+                     unsigned nb1) {
+    extern __shared__ unsigned sm[];
+    __shared__ unsigned warp_tot[kPartThreads / 32];
+    __shared__ long long s_b0;
+    __shared__ unsigned s_len, s_base, s_nb;
+    unsigned *hist = sm;                     // counts, then running slot cursors
+    unsigned *lstart = hist + kMaxPassBins;  // local exclusive starts
+    unsigned *gbase = lstart + kMaxPassBins; // reserved global starts
+    unsigned *sdig = gbase + kMaxPassBins;   // digit of each staged slot
+    unsigned *stage = sdig + kBatch;         // [fields][kBatch]
+
+    if (threadIdx.x == 0) {
+        if (PASS == 1) {
+            s_b0 = (long long)blockIdx.x * kBatch;
+            const long long rem = n - s_b0;
+            s_len = rem < kBatch ? (unsigned)(rem > 0 ? rem : 0) : kBatch;
+            s_base = 0;
+            s_nb = FINAL ? B : nb1;
+        } else {
+            // bucket of this batch: largest b with batch_off[b] <= blockIdx.x
+            unsigned lo = 0, hi = nb1;
+            while (lo < hi) {
+                const unsigned mid = (lo + hi + 1) / 2;
+                if (batch_off[mid] <= blockIdx.x) lo = mid;
+                else hi = mid - 1;
+            }
+            const unsigned b = lo;
+            if (b >= nb1) {
+                s_len = 0;
+            } else {
+                const unsigned t0 = b * tpb;
+                const unsigned t1 = min(t0 + tpb, B);
+                const long long start = offs[t0];
+                const long long end = t1 < B ? (long long)offs[t1] : n;
+                s_b0 = start + (long long)(blockIdx.x - batch_off[b]) * kBatch;
+                const long long rem = end - s_b0;
+                s_len = rem < kBatch ? (unsigned)(rem > 0 ? rem : 0) : kBatch;
+                s_base = t0;
+                s_nb = t1 - t0;
+            }
+        }
+    }
+    for (unsigned d = threadIdx.x; d < kMaxPassBins; d += kPartThreads) hist[d] = 0;
+    __syncthreads();
+    const unsigned len = s_len;
+    if (len == 0) return;
+    const long long b0 = s_b0;
+    const unsigned base = s_base, nb = s_nb;
+
+    // load the batch into registers (coalesced), count digits
+    unsigned dig[kItems], key[kItems], val[kItems][kMaxPayload];
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        const unsigned idx = threadIdx.x + i * kPartThreads;
+        dig[i] = 0xffffffffu;
+        if (idx < len) {
+            const long long p = b0 + idx;
+            unsigned k;
+            if (PASS == 1) k = tile_key<DIM, TILE>(g, kx[p], ky[p], DIM == 3 ? kz[p] : 0.f);
+            else k = in_key[p];
+            key[i] = k;
+            unsigned d = (PASS == 1) ? (FINAL ? k : k / tpb) : k - base;
+            if (d >= nb) d = nb - 1;  // defensive: never index outside the histogram
+            dig[i] = d;
+#pragma unroll
+            for (int f = 0; f < kMaxPayload; ++f)
+                if (f < np) val[i][f] = pl.in[f][p];
+            atomicAdd(&hist[d], 1u);
+        }
+    }
+    __syncthreads();
+    // local starts and one global reservation per non-empty digit
+    for (unsigned d = threadIdx.x; d < kMaxPassBins; d += kPartThreads) lstart[d] = hist[d];
+    __syncthreads();
+    block_exclusive_scan(lstart, nb, warp_tot);
+    for (unsigned d = threadIdx.x; d < nb; d += kPartThreads) {
+        const unsigned c = hist[d];
+        gbase[d] = c ? atomicAdd(&gcursor[base + d], c) : 0u;
+        hist[d] = lstart[d];
+    }
+    __syncthreads();
+    // rank inside the batch and stage in shared memory
+    const int nf = np + ((PASS == 1 && !FINAL) ? 1 : 0);
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        if (dig[i] == 0xffffffffu) continue;
+        const unsigned slot = atomicAdd(&hist[dig[i]], 1u);
+        sdig[slot] = dig[i];
+#pragma unroll
+        for (int f = 0; f < kMaxPayload; ++f)
+            if (f < np) stage[f * kBatch + slot] = val[i][f];
+        if (PASS == 1 && !FINAL) stage[np * kBatch + slot] = key[i];
+    }
+    __syncthreads();
+    // write every digit's run with consecutive threads
+    for (unsigned slot = threadIdx.x; slot < len; slot += kPartThreads) {
+        const unsigned d = sdig[slot];
+        const unsigned gpos = gbase[d] + (slot - lstart[d]);
+        for (int f = 0; f < nf; ++f) {
+            const unsigned v = stage[f * kBatch + slot];
+            if (f < np) {
+                pl.out[f][gpos] = v;  // the intermediate arrays in pass 1, the output otherwise
+            } else {
+                out_key[gpos] = v;
+            }
+        }
+    }
+}
+
+// cursor1[b] = start of bucket b; cursor2[t] = start of tile t (written by the
+// scan); batch_off = exclusive scan of the per-bucket batch counts.
+__global__ void __launch_bounds__(1024)
+    bucket_setup_kernel(const uint32_t *__restrict__ offs, long long n, unsigned B, unsigned tpb,
+                        unsigned nb1, unsigned *__restrict__ cursor1, unsigned *__restrict__ batch_off) {
+    __shared__ unsigned cnt[kMaxBuckets + 1];
+    const unsigned b = threadIdx.x;
+    if (b < nb1) {
+        const unsigned t0 = b * tpb, t1 = min(t0 + tpb, B);
+        const long long start = offs[t0];
+        const long long end = t1 < B ? (long long)offs[t1] : n;
+        cursor1[b] = (unsigned)start;
+        const long long size = end > start ? end - start : 0;
+        cnt[b] = (unsigned)((size + kBatch - 1) / kBatch);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned run = 0;
+        for (unsigned i = 0; i < nb1; ++i) {
+            batch_off[i] = run;
+            run += cnt[i];
+        }
+        batch_off[nb1] = run;
+    }
+}
+
+enum Path { kChunked = 0, kGlobal = 1, kTwoPass = 2 };
+
 struct Plan {
-    bool chunked;
+    int path;
     unsigned B;
-    unsigned G;        // chunks (chunked path)
+    unsigned G;        // chunks (chunked path and the chunked count of the two-pass path)
     long long chunk;   // particles per chunk
+    unsigned tpb, nb1; // two-pass: tiles per bucket, buckets (1 = single pass)
     size_t bytes;      // workspace bytes
-    size_t smem;       // dynamic shared memory of count / scatter
+    size_t smem;       // dynamic shared memory of the chunked count / scatter
+    // workspace layout (byte offsets)
+    size_t o_counts, o_totals, o_cursor, o_cursor1, o_batch, o_inter, o_key;
 };
 
-Plan make_plan(const TileGrid &tg, long long n) {
+// Path choice.  The chunked path writes each (chunk, bin) run 4 bytes at a
+// time as its particles arrive, so every run keeps one partly written sector
+// per payload field open; that is fine while the whole output stays in L2.  For
+// larger outputs the open sectors are evicted half written and DRAM does
+// read-modify-write on every sector, so the two-pass partition is used.
+constexpr double kL2Resident = 96.0 * 1024 * 1024;
+
+Plan make_plan(const TileGrid &tg, long long n, int n_payload) {
     Plan p{};
     p.B = (unsigned)(tg.n_tiles + 1);
-    p.chunked = p.B <= kSmemBins;
-    if (p.chunked) {
+    const double out = (double)n * n_payload * 4.0;
+    const bool small_bins = p.B <= kSmemBins;
+    if (out <= kL2Resident) p.path = small_bins ? kChunked : kGlobal;
+    else p.path = kTwoPass;
+    if (p.path == kTwoPass) {
+        if (p.B <= kMaxPassBins) {
+            p.nb1 = 1;
+            p.tpb = p.B;
+        } else {
+            p.tpb = (p.B + kMaxBuckets - 1) / kMaxBuckets;
+            if (p.tpb > kMaxPassBins) p.path = kGlobal;  // too many bins for two passes
+            p.nb1 = (p.B + p.tpb - 1) / p.tpb;
+        }
+    }
+    // chunked counting (used by the chunked path and to count for the two-pass path)
+    if (small_bins) {
         p.smem = (size_t)p.B * sizeof(unsigned);
-        // resident CTAs per SM allowed by shared memory (228 KB per SM, 1 KB reserved per CTA)
         long long per_sm = (228 * 1024) / (long long)(p.smem + 1024);
         if (per_sm < 1) per_sm = 1;
         if (per_sm > 4) per_sm = 4;
         long long G = (long long)kNumSMs * per_sm;
-        long long max_g = (n + 1023) / 1024;  // at least ~1024 particles per chunk
+        long long max_g = (n + 1023) / 1024;
         if (max_g < 1) max_g = 1;
         if (G > max_g) G = max_g;
         p.G = (unsigned)G;
         p.chunk = (n + G - 1) / G;
         if (p.chunk < 1) p.chunk = 1;
-        p.bytes = align_up((size_t)G * p.B * sizeof(unsigned), 256) +
-                  align_up((size_t)p.B * sizeof(unsigned), 256);
-    } else {
-        p.smem = 0;
-        p.G = 0;
-        p.chunk = 0;
-        p.bytes = 2 * align_up((size_t)p.B * sizeof(unsigned), 256);
     }
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += align_up(bytes, 256);
+        return at;
+    };
+    const size_t b4 = (size_t)p.B * sizeof(unsigned);
+    if (p.path == kChunked) {
+        p.o_counts = take((size_t)p.G * b4);
+        p.o_totals = take(b4);
+    } else if (p.path == kGlobal) {
+        p.o_totals = take(b4);
+        p.o_cursor = take(b4);
+    } else {
+        if (small_bins) p.o_counts = take((size_t)p.G * b4);
+        p.o_totals = take(b4);
+        p.o_cursor = take(b4);
+        p.o_cursor1 = take((kMaxBuckets + 1) * sizeof(unsigned));
+        p.o_batch = take((kMaxBuckets + 1) * sizeof(unsigned));
+        if (p.nb1 > 1) {
+            p.o_inter = take((size_t)n * n_payload * 4);
+            p.o_key = take((size_t)n * 4);
+        }
+    }
+    p.bytes = o;
     return p;
+}
+
+template <int DIM, int TILE>
+pcg_status count_into_totals(const KeyGeom &g, const Plan &pl, long long n, const float *const *kp,
+                             unsigned char *ws, unsigned long long *n_invalid, cudaStream_t s) {
+    const float *kz = DIM == 3 ? kp[2] : kp[0];
+    unsigned *totals = reinterpret_cast<unsigned *>(ws + pl.o_totals);
+    if (pl.B <= kSmemBins) {
+        unsigned *counts = reinterpret_cast<unsigned *>(ws + pl.o_counts);
+        if (pl.smem > 48 * 1024)
+            PCG_CHECK_CUDA(cudaFuncSetAttribute(count_chunked_kernel<DIM, TILE>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)pl.smem));
+        {
+            prof::Mark mk("sort_count", s);
+            count_chunked_kernel<DIM, TILE><<<pl.G, kSortThreads, pl.smem, s>>>(
+                g, kp[0], kp[1], kz, n, pl.chunk, counts, pl.B, n_invalid);
+        }
+        PCG_CHECK_LAUNCH();
+        prof::Mark mk("sort_colscan", s);
+        colscan_kernel<<<(pl.B + 255) / 256, 256, 0, s>>>(counts, totals, pl.G, pl.B);
+        return launch_status();
+    }
+    pcg_status st = zero_f32(reinterpret_cast<float *>(totals), pl.B, s);
+    if (st != PCG_OK) return st;
+    prof::Mark mk("sort_count_global", s);
+    count_global_kernel<DIM, TILE><<<(unsigned)kNumSMs * 8, 256, 0, s>>>(g, kp[0], kp[1], kz, n,
+                                                                        totals, n_invalid);
+    return launch_status();
 }
 
 template <int DIM, int TILE>
@@ -249,57 +525,78 @@ pcg_status run_sort(const TileGrid &tg, const Plan &pl, long long n, const float
     g.N2 = (float)tg.N[2];
     g.tile = tg.tile;
     const float *kz = DIM == 3 ? kp[2] : kp[0];
-    if (pl.chunked) {
-        unsigned *counts = reinterpret_cast<unsigned *>(ws);
-        unsigned *totals = reinterpret_cast<unsigned *>(
-            ws + align_up((size_t)pl.G * pl.B * sizeof(unsigned), 256));
-        if (pl.smem > 48 * 1024) {
-            PCG_CHECK_CUDA(cudaFuncSetAttribute(count_chunked_kernel<DIM, TILE>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)pl.smem));
-            PCG_CHECK_CUDA(cudaFuncSetAttribute(scatter_chunked_kernel<DIM, TILE>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                (int)pl.smem));
-        }
-        {
-            prof::Mark mk("sort_count", s);
-            count_chunked_kernel<DIM, TILE><<<pl.G, kSortThreads, pl.smem, s>>>(
-                g, kp[0], kp[1], kz, n, pl.chunk, counts, pl.B, n_invalid);
-        }
-        PCG_CHECK_LAUNCH();
-        {
-            prof::Mark mk("sort_colscan", s);
-            colscan_kernel<<<(pl.B + 255) / 256, 256, 0, s>>>(counts, totals, pl.G, pl.B);
-        }
-        PCG_CHECK_LAUNCH();
+    pcg_status st = count_into_totals<DIM, TILE>(g, pl, n, kp, ws, n_invalid, s);
+    if (st != PCG_OK) return st;
+    unsigned *totals = reinterpret_cast<unsigned *>(ws + pl.o_totals);
+    if (pl.path == kChunked) {
+        unsigned *counts = reinterpret_cast<unsigned *>(ws + pl.o_counts);
         {
             prof::Mark mk("sort_scan", s);
             scan_one_cta_kernel<<<1, 1024, 0, s>>>(totals, offs, nullptr, pl.B);
         }
         PCG_CHECK_LAUNCH();
+        if (pl.smem > 48 * 1024)
+            PCG_CHECK_CUDA(cudaFuncSetAttribute(scatter_chunked_kernel<DIM, TILE>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)pl.smem));
         prof::Mark mk("sort_scatter", s);
         scatter_chunked_kernel<DIM, TILE><<<pl.G, kSortThreads, pl.smem, s>>>(
             g, kp[0], kp[1], kz, n, pl.chunk, counts, offs, pl.B, py, np);
         return launch_status();
     }
-    unsigned *totals = reinterpret_cast<unsigned *>(ws);
-    unsigned *cursor =
-        reinterpret_cast<unsigned *>(ws + align_up((size_t)pl.B * sizeof(unsigned), 256));
-    pcg_status st = zero_f32(reinterpret_cast<float *>(totals), pl.B, s);
-    if (st != PCG_OK) return st;
-    const unsigned grid = (unsigned)kNumSMs * 8;
-    {
-        prof::Mark mk("sort_count_global", s);
-        count_global_kernel<DIM, TILE><<<grid, 256, 0, s>>>(g, kp[0], kp[1], kz, n, totals, n_invalid);
-    }
-    PCG_CHECK_LAUNCH();
+    unsigned *cursor = reinterpret_cast<unsigned *>(ws + pl.o_cursor);
     {
         prof::Mark mk("sort_scan", s);
         scan_one_cta_kernel<<<1, 1024, 0, s>>>(totals, offs, cursor, pl.B);
     }
     PCG_CHECK_LAUNCH();
-    prof::Mark mk("sort_scatter_global", s);
-    scatter_global_kernel<DIM, TILE><<<grid, 256, 0, s>>>(g, kp[0], kp[1], kz, n, cursor, py, np);
+    if (pl.path == kGlobal) {
+        prof::Mark mk("sort_scatter_global", s);
+        scatter_global_kernel<DIM, TILE><<<(unsigned)kNumSMs * 8, 256, 0, s>>>(g, kp[0], kp[1], kz, n,
+                                                                              cursor, py, np);
+        return launch_status();
+    }
+    // two-pass partition
+    const size_t smem = (size_t)(3 * kMaxPassBins + kBatch) * 4 + (size_t)(np + 1) * kBatch * 4;
+    const unsigned grid1 = (unsigned)((n + kBatch - 1) / kBatch);
+    if (pl.nb1 == 1) {
+        PCG_CHECK_CUDA(cudaFuncSetAttribute(partition_kernel<DIM, TILE, 1, true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        prof::Mark mk("sort_partition", s);
+        partition_kernel<DIM, TILE, 1, true><<<grid1, kPartThreads, smem, s>>>(
+            g, kp[0], kp[1], kz, n, py, np, nullptr, nullptr, cursor, 1, pl.B, nullptr, offs, 1);
+        return launch_status();
+    }
+    unsigned *cursor1 = reinterpret_cast<unsigned *>(ws + pl.o_cursor1);
+    unsigned *batch = reinterpret_cast<unsigned *>(ws + pl.o_batch);
+    unsigned *ikey = reinterpret_cast<unsigned *>(ws + pl.o_key);
+    Payload p1{}, p2{};
+    for (int f = 0; f < np; ++f) {
+        unsigned *inter = reinterpret_cast<unsigned *>(ws + pl.o_inter + (size_t)f * n * 4);
+        p1.in[f] = py.in[f];
+        p1.out[f] = inter;
+        p2.in[f] = inter;
+        p2.out[f] = py.out[f];
+    }
+    {
+        prof::Mark mk("sort_bucket_setup", s);
+        bucket_setup_kernel<<<1, 1024, 0, s>>>(offs, n, pl.B, pl.tpb, pl.nb1, cursor1, batch);
+    }
+    PCG_CHECK_LAUNCH();
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(partition_kernel<DIM, TILE, 1, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(partition_kernel<DIM, TILE, 2, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    {
+        prof::Mark mk("sort_partition1", s);
+        partition_kernel<DIM, TILE, 1, false><<<grid1, kPartThreads, smem, s>>>(
+            g, kp[0], kp[1], kz, n, p1, np, nullptr, ikey, cursor1, pl.tpb, pl.B, batch, offs, pl.nb1);
+    }
+    PCG_CHECK_LAUNCH();
+    const unsigned grid2 = grid1 + pl.nb1;  // upper bound on the bucket-aligned batches
+    prof::Mark mk("sort_partition2", s);
+    partition_kernel<DIM, TILE, 2, false><<<grid2, kPartThreads, smem, s>>>(
+        g, kp[0], kp[1], kz, n, p2, np, ikey, nullptr, cursor, pl.tpb, pl.B, batch, offs, pl.nb1);
     return launch_status();
 }
 
@@ -325,11 +622,12 @@ bool valid_sort_args(int32_t dim, const int32_t *grid, int32_t tile, int64_t n, 
 }  // namespace pcg
 
 extern "C" pcg_status pcg_tile_sort_workspace_size(int32_t dim, const int32_t *grid, int32_t tile,
-                                                   int64_t n, size_t *bytes) {
+                                                   int64_t n, int32_t n_payload, size_t *bytes) {
     using namespace pcg;
     TileGrid tg;
     if (bytes == nullptr || !valid_sort_args(dim, grid, tile, n, &tg)) return PCG_ERR_INVALID_ARG;
-    *bytes = make_plan(tg, n).bytes;
+    if (n_payload < 1 || n_payload > kMaxPayload) return PCG_ERR_INVALID_ARG;
+    *bytes = make_plan(tg, n, n_payload).bytes;
     return PCG_OK;
 }
 
@@ -353,7 +651,7 @@ extern "C" pcg_status pcg_tile_sort(int32_t dim, const int32_t *grid, int32_t ti
     }
     for (int mu = 0; mu < dim; ++mu)
         if (n > 0 && key_pos[mu] == nullptr) return PCG_ERR_INVALID_ARG;
-    const Plan pl = make_plan(tg, n);
+    const Plan pl = make_plan(tg, n, n_payload);
     if (workspace_bytes < pl.bytes || (pl.bytes > 0 && workspace == nullptr))
         return PCG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return PCG_ERR_WORKSPACE;

@@ -70,14 +70,15 @@ def test_cic1d_rejects_bad_arguments(lib):
 def test_workspace_queries(lib):
     out = ctypes.c_size_t(0)
     # 3D 256^3 with tile 8: 32768 tiles + sentinel, block-private counters
-    assert lib.pcg_tile_sort_workspace_size(3, _grid(256, 256, 256), 8, 268435456, ctypes.byref(out)) == 0
-    assert out.value > 32769 * 4
+    assert lib.pcg_tile_sort_workspace_size(3, _grid(256, 256, 256), 8, 268435456, 7, ctypes.byref(out)) == 0
+    assert out.value > 268435456 * 8 * 4  # two-pass: intermediate payload + key
     # one bin per cell of 64^3: global counters (two arrays of 262145 entries)
-    assert lib.pcg_tile_sort_workspace_size(3, _grid(64, 64, 64), 1, 16777216, ctypes.byref(out)) == 0
+    assert lib.pcg_tile_sort_workspace_size(3, _grid(64, 64, 64), 1, 100000, 7, ctypes.byref(out)) == 0
     assert out.value == 2 * ((262145 * 4 + 255) // 256 * 256)
-    assert lib.pcg_tile_sort_workspace_size(4, _grid(8, 8, 8), 8, 10, ctypes.byref(out)) == 1
-    assert lib.pcg_tile_sort_workspace_size(3, _grid(8, 0, 8), 8, 10, ctypes.byref(out)) == 1
-    assert lib.pcg_tile_sort_workspace_size(3, _grid(8, 8, 8), 0, 10, ctypes.byref(out)) == 1
+    assert lib.pcg_tile_sort_workspace_size(4, _grid(8, 8, 8), 8, 10, 1, ctypes.byref(out)) == 1
+    assert lib.pcg_tile_sort_workspace_size(3, _grid(8, 0, 8), 8, 10, 1, ctypes.byref(out)) == 1
+    assert lib.pcg_tile_sort_workspace_size(3, _grid(8, 8, 8), 0, 10, 1, ctypes.byref(out)) == 1
+    assert lib.pcg_tile_sort_workspace_size(3, _grid(8, 8, 8), 8, 10, 0, ctypes.byref(out)) == 1
     assert lib.pcg_deposit_current_workspace_size(3, _grid(16, 16, 16), 8, 100000, ctypes.byref(out)) == 0
     assert out.value >= 4 and out.value % 256 == 0
     assert lib.pcg_assemble_mass_matrix_workspace_size(_grid(64, 64, 64), 16, ctypes.byref(out)) == 0

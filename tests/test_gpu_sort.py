@@ -56,6 +56,16 @@ def test_sort_global_path(grid, tile, n):
     _check_sort(pcg, grid, tile, _particles(rng, grid, n))
 
 
+@pytest.mark.parametrize("grid,tile", [((64, 64, 64), 8), ((128, 128, 128), 4), ((64, 64, 64), 1),
+                                       ((700, 700), 8)])
+def test_sort_partition_passes(grid, tile):
+    # outputs larger than L2 (9 M particles x 3-4 fields here): one partition
+    # pass for <= 2048 bins, else two passes (coarse buckets, then tiles)
+    pcg = need_gpu()
+    rng = np.random.default_rng(sum(grid) + tile)
+    _check_sort(pcg, grid, tile, _particles(rng, grid, 9_000_001, invalid=1001))
+
+
 @pytest.mark.parametrize("grid,tile", [((32, 32, 32), 8), ((50, 50, 50), 1)])
 def test_sort_invalid_particles_go_to_the_tail(grid, tile):
     pcg = need_gpu()
