@@ -96,6 +96,11 @@ __device__ __forceinline__ void red_add_v4_f32(float *addr, float a, float b, fl
                  : "memory");
 }
 
+// Ask for [p, p + bytes) to be brought into L2 (bytes a multiple of 16, p 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, unsigned bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Fire-and-forget fp32 add into shared memory (red.shared.add.f32).
 __device__ __forceinline__ void red_shared_add_f32(float *addr, float v) {
     unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(addr));

@@ -109,7 +109,10 @@ __device__ __forceinline__ void deposit_global(const Geom &g, float *__restrict_
 // period below (a particle that drifted across the lower periodic boundary).
 template <int S, int TILE, int HALO>
 __device__ __forceinline__ int local_index(int f, int origin, int N) {
-    int d = (f - origin) % N;
+    // f in [-1, N) (a first node of an in-domain particle) and origin in [0, N),
+    // so f - origin lies in [-N - 1, N) and at most two corrections reduce it
+    int d = f - origin;
+    if (d < 0) d += N;
     if (d < 0) d += N;
     return d + S - 1 < TILE + HALO ? d : d - N;
 }
