@@ -315,17 +315,17 @@ def cpu_baseline_current(d, budget_s=12.0):
                       f"fp64 C oracle single thread, {dt:.1f} s"}
 
 
-def mass_workload(pcg, steps, warmup, dist, peaks, traffic):
+def mass_workload(pcg, steps, warmup, dist, peaks, traffic, edge=64):
     import torch
     import synth
-    d = synth.mass3d()
+    d = synth.mass3d(grid=(edge, edge, edge))
     grid, n = d["grid"], d["n"]
     dev = lambda a: torch.from_numpy(a).cuda()
     dp = [dev(p) for p in d["pos"]]
     out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(d["w"])] + [dev(o) for o in d["omega"]])
     M = torch.empty(tuple(reversed(grid)) + (27, 3, 3), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
-    res = {"workload": "mass3d 64^3 x 64 ppc (CIC, 27 offsets x 3x3 blocks)", "particles": n}
+    res = {"workload": f"mass3d {edge}^3 x 64 ppc (CIC, 27 offsets x 3x3 blocks)", "particles": n}
     alg_bytes = n * 28 + M.numel() * 4
     useful_flops = n * 8 * 8 * 9 * 2
     issued = {"tf32": n * 128 * 16 * 2, "bf16": n * 128 * 16 * 2, "simt": 0}
@@ -436,6 +436,27 @@ def run_gpu(args):
     dist.close()
 
 
+def run_only(args):
+    """One secondary workload alone (a profiling aid; not the benchmark line)."""
+    import torch
+    import particle_cell_grid_gb300 as pcg
+    import synth
+    dist = Dist(1)
+    torch.cuda.set_device(0)
+    pcg._lib.load()
+    peaks, _ = load_peaks()
+    traffic = load_traffic()
+    if args.only == "mass":
+        out = mass_workload(pcg, args.steps, args.warmup, dist, peaks, traffic, edge=args.mass_grid)
+    elif args.only == "cic1d":
+        out = cic1d_workload(pcg, args.steps, args.warmup, dist)
+    else:
+        d = synth.quad3d_bump() if args.only == "quad" else synth.cic2d()
+        out = current_workload(pcg, d, args.steps, args.warmup, dist, peaks, traffic)
+        out.pop("profile", None)
+    print(json.dumps({"only": args.only, **out}), flush=True)
+
+
 def run_reference(args):
     """The oracle as it stands on the host cores, on bounded samples of the same workload."""
     dist = Dist(args.gpus)
@@ -484,11 +505,16 @@ def main():
     ap.add_argument("--grid", type=int, default=256, help="edge of the headline workload's grid (256 = full size)")
     ap.add_argument("--main-only", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--only", choices=["mass", "quad", "cic2d", "cic1d"], default=None,
+                    help="time one secondary workload alone and print its figures (for profiling)")
+    ap.add_argument("--mass-grid", type=int, default=64, help="edge of the mass-matrix grid")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_gpu(args)
 

@@ -13,20 +13,25 @@
 //
 // GB300 design.
 //  * One tcgen05.mma per K-step computes all nine tensor components of a cell
-//    at once: A stacks the nine 8 x K blocks W S^{ij} into its rows (row
+//    batch at once: A stacks the nine 8 x K blocks W S^{ij} into its rows (row
 //    r = 8*(3i+j) + a; 72 of the 128 rows of an M = 128 MMA), B = W^T is K x 8
-//    (N = 16; columns 8..15 and rows 72..127 are never read back, so their
-//    shared-memory footprint overlaps the next buffer instead of being zeroed).
-//    TF32 (kind::tf32, K = 8 per instruction) or BF16 (kind::f16, K = 16), fp32
-//    accumulation in tensor memory; one thread issues, the result comes back
-//    with tcgen05.ld (32 lanes x 8 columns per warp).
+//    (N = 16).  Rows 72..127 of A and columns 8..15 of B are never read back, so
+//    their shared-memory footprint overlaps the next buffer instead of being
+//    zeroed.  TF32 (kind::tf32, K = 8 per instruction) or BF16 (kind::f16,
+//    K = 16), fp32 accumulation in tensor memory; one thread issues, the result
+//    comes back with tcgen05.ld (32 lanes x 8 columns per warp).
+//  * Operands use the 128-byte-swizzled K-major layout.  Two threads own one
+//    particle (one K column of A and B; tensor components 0-4 and B, or 5-8):
+//    a warp's 32 consecutive particles write a full 128-byte row per store
+//    instruction, all 32 banks, with the row index a compile-time constant, so
+//    the particle's corner weights and coefficients stay in registers.
+//  * The next batch group's particles are loaded into registers while the
+//    tensor core runs on the current one.
 //  * A CTA walks 4x4x4-cell blocks; each block's 5x5x5 node window of
 //    243-float blocks (121.5 KB) is accumulated in shared memory and flushed
-//    once to global M with 16-byte vector reductions, so global reduction
-//    traffic is ~1.95 node blocks per cell instead of 8.
-//  * Operands are written in the canonical K-major no-swizzle layout (8 rows x
-//    16 bytes per core matrix) with a rotated row order per thread, so each
-//    8-thread store phase hits 32 distinct banks.
+//    once to global M, ~1.95 node blocks of reductions per cell instead of 8:
+//    each window row (5 nodes, contiguous in M) goes out as one asynchronous
+//    bulk reduce-add on the TMA engine, issued by one thread.
 //  * precision 2 computes the same local products on CUDA cores (fp32 FMAs),
 //    the A/B baseline of the tensor-core kernel.
 #include <cuda_bf16.h>
@@ -37,13 +42,15 @@
 namespace pcg {
 namespace mm {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int KB = 64;             // particles per batch: the K extent of one cell product
 constexpr int G = 4;               // batches (cell products) per iteration
 constexpr int BC = 4;              // cell-block edge
 constexpr int WN = BC + 1;         // node-window edge
-constexpr int WNODES = WN * WN * WN;
-constexpr int ACC_FLOATS = WNODES * 243;
+// A window row of 5 node blocks (1215 floats) starts 0-3 floats into its 1220-float
+// slot, so that it has the same alignment modulo 16 bytes as its place in M.
+constexpr int ACC_ROW = 1220;
+constexpr int ACC_FLOATS = WN * WN * ACC_ROW;
 constexpr int ACC_BYTES = (ACC_FLOATS * 4 + 1023) / 1024 * 1024;
 constexpr uint32_t kTmemCols = 64;  // G accumulators of 16 columns
 constexpr uint32_t kMaxPolls = 1u << 22;
@@ -51,17 +58,23 @@ constexpr unsigned kFlagTimeout = 4u;
 
 enum Mode { TF32 = 0, BF16 = 1, SIMT = 2 };
 
+// Staging of one batch (128-byte swizzle, K-major):
+//   TF32: K = 64 x 4 B = 256 B per row = two 128-byte K-atoms; per K-atom the 72
+//         A rows are 9 atoms of 8 rows (9 KB), B's 8 rows one atom (1 KB).
+//         [A k0 | A k1 | B k0 | B k1] = 20 KB.
+//   BF16: K = 64 x 2 B = one K-atom.  [A | B] = 10 KB.
 template <int MODE>
 struct Op {
-    static constexpr int EPC = MODE == TF32 ? 4 : 8;  // K elements per 16-byte core-matrix row
-    static constexpr int KG = KB / EPC;               // core matrices along K
-    static constexpr int SBO = KG * 128;              // stride between 8-row groups
-    static constexpr int A_BYTES = 9 * SBO;           // rows 0..71
-    static constexpr int B_BYTES = SBO;               // N rows 0..7
+    static constexpr int KATOMS = MODE == TF32 ? 2 : 1;
+    static constexpr int A_KSTRIDE = 9 * 1024;               // A bytes per K-atom
+    static constexpr int A_BYTES = KATOMS * A_KSTRIDE;
+    static constexpr int B_BYTES = KATOMS * 1024;
     static constexpr int BATCH = A_BYTES + B_BYTES;
-    static constexpr int STAGING = G * BATCH + 7 * SBO;  // rows 72..127 of the last A stay inside
+    // the MMA reads 16 row atoms of A and 2 of B from each K-atom base: the last
+    // batch's reads run up to 7 KB past its A and 1 KB past its B
+    static constexpr int STAGING = G * BATCH + 8 * 1024;
     static constexpr int KSTEPS = MODE == TF32 ? KB / 8 : KB / 16;
-    static constexpr int PARTS = kThreads / (G * KG);  // threads sharing one k-group
+    static constexpr int EB = MODE == TF32 ? 4 : 2;           // element bytes
 };
 
 template <>
@@ -128,45 +141,107 @@ __device__ void particle_global(const Args &A, float x, float y, float z, float 
     }
 }
 
-// Load one particle; returns false (weights zero) when it is padding.  A
-// particle outside its listed cell is flagged and deposited by the slow path
-// (only by the thread with `owner` set, so exactly once).
-__device__ __forceinline__ bool load_particle(const Args &A, const Batch &b, int k, int cx, int cy,
-                                              int cz, bool owner, float &fx, float &fy, float &fz,
-                                              float (&s)[9]) {
-    if (b.ci < 0 || k >= (int)b.len) return false;
-    const unsigned p = b.start + k;
-    const float x = A.x[p], y = A.y[p], z = A.z[p];
-    const float w = A.w[p], ox = A.ox[p], oy = A.oy[p], oz = A.oz[p];
-    const bool inside = x >= (float)cx && x < (float)(cx + 1) && y >= (float)cy &&
-                        y < (float)(cy + 1) && z >= (float)cz && z < (float)(cz + 1);
-    if (!inside) {
-        if (owner) {
-            const bool ok = x >= 0.f && x < (float)A.N[0] && y >= 0.f && y < (float)A.N[1] &&
-                            z >= 0.f && z < (float)A.N[2];
-            if (ok) particle_global(A, x, y, z, w, ox, oy, oz);
-            if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
+// This thread's particle of the batch group: raw fields, loaded ahead of use.
+struct Raw {
+    float x, y, z, w, ox, oy, oz;
+    bool live;
+};
+
+__device__ __forceinline__ Raw load_raw(const Args &A, const Batch &b, int k) {
+    Raw r;
+    r.live = b.ci >= 0 && k < (int)b.len;
+    if (r.live) {
+        const unsigned p = b.start + k;
+        r.x = A.x[p];
+        r.y = A.y[p];
+        r.z = A.z[p];
+        r.w = A.w[p];
+        r.ox = A.ox[p];
+        r.oy = A.oy[p];
+        r.oz = A.oz[p];
+    } else {
+        r.x = r.y = r.z = r.w = r.ox = r.oy = r.oz = 0.f;
+    }
+    return r;
+}
+
+// Weights and coefficients of a loaded particle for the cell (cx, cy, cz); a
+// particle outside that cell is flagged, deposited by the slow path and
+// contributes zeros here.
+__device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int cy, int cz,
+                                        bool owner, float (&W)[8], float (&s)[9]) {
+    bool use = r.live;
+    if (use) {
+        const bool inside = r.x >= (float)cx && r.x < (float)(cx + 1) && r.y >= (float)cy &&
+                            r.y < (float)(cy + 1) && r.z >= (float)cz && r.z < (float)(cz + 1);
+        if (!inside) {
+            const bool ok = r.x >= 0.f && r.x < (float)A.N[0] && r.y >= 0.f && r.y < (float)A.N[1] &&
+                            r.z >= 0.f && r.z < (float)A.N[2];
+            if (owner) {  // once per particle, by one of the threads sharing it
+                if (ok) particle_global(A, r.x, r.y, r.z, r.w, r.ox, r.oy, r.oz);
+                if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
+            }
+            use = false;
         }
+    }
+    if (!use) {
+#pragma unroll
+        for (int a = 0; a < 8; ++a) W[a] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 9; ++c) s[c] = 0.f;
         return false;
     }
-    fx = x - (float)cx;
-    fy = y - (float)cy;
-    fz = z - (float)cz;
-    alpha_w(w, ox, oy, oz, s);
+    const float fx = r.x - (float)cx, fy = r.y - (float)cy, fz = r.z - (float)cz;
+    const float gx = 1.f - fx, gy = 1.f - fy, gz = 1.f - fz;
+    const float yz00 = gy * gz, yz10 = fy * gz, yz01 = gy * fz, yz11 = fy * fz;
+    W[0] = gx * yz00;
+    W[1] = fx * yz00;
+    W[2] = gx * yz10;
+    W[3] = fx * yz10;
+    W[4] = gx * yz01;
+    W[5] = fx * yz01;
+    W[6] = gx * yz11;
+    W[7] = fx * yz11;
+    alpha_w(r.w, r.ox, r.oy, r.oz, s);
     return true;
+}
+
+// The G batches starting at cursor (cur, cur_k); identical in every thread.
+__device__ __forceinline__ bool next_batches(const unsigned *cstart, const unsigned *ccount, int &cur,
+                                             unsigned &cur_k, Batch (&bt)[G]) {
+    bool any = false;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+        while (cur < 64 && cur_k >= ccount[cur]) {
+            ++cur;
+            cur_k = 0;
+        }
+        if (cur < 64) {
+            const unsigned rem = ccount[cur] - cur_k;
+            bt[j] = Batch{cur, cstart[cur] + cur_k, rem < (unsigned)KB ? rem : (unsigned)KB};
+            cur_k += KB;
+            any = true;
+        } else {
+            bt[j] = Batch{-1, 0, 0};
+        }
+    }
+    return any;
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
     extern __shared__ __align__(1024) unsigned char smem[];
-    float *acc = reinterpret_cast<float *>(smem);
-    unsigned char *stage = smem + ACC_BYTES;
-    unsigned *cstart = reinterpret_cast<unsigned *>(stage + Op<MODE>::STAGING);
+    unsigned char *stage = smem;  // 1024-aligned operand staging first
+    float *acc = reinterpret_cast<float *>(smem + Op<MODE>::STAGING);
+    unsigned *cstart = reinterpret_cast<unsigned *>(smem + Op<MODE>::STAGING + ACC_BYTES);
     unsigned *ccount = cstart + 64;
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(ccount + 64);
+    int *rsh = reinterpret_cast<int *>(ccount + 64);  // window row shifts (floats)
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(rsh + 32);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mbar + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int pme = tid % (G * KB), half = tid / (G * KB);
+    const int jme = pme / KB, kme = pme % KB;  // this thread's batch, particle and half
     uint32_t tmem = 0;
     if (MODE != SIMT) {
         if (warp == 0) tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -201,96 +276,56 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
             }
             cstart[tid] = s;
             ccount[tid] = c;
+        } else if (tid < 64 + WN * WN) {
+            const int row = tid - 64;
+            const int gy = (by * BC + row % WN) % A.N[1], gz = (bz * BC + row / WN) % A.N[2];
+            const long long node = ((long long)gz * A.N[1] + gy) * A.N[0] + (bx * BC) % A.N[0];
+            rsh[row] = (int)((node * 243) & 3);
         }
         __syncthreads();
 
         int cur = 0;
         unsigned cur_k = 0;
-        while (true) {
-            // the next G batches (identical in every thread)
-            Batch bt[G];
-            bool any = false;
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                while (cur < 64 && cur_k >= ccount[cur]) {
-                    ++cur;
-                    cur_k = 0;
-                }
-                if (cur < 64) {
-                    const unsigned rem = ccount[cur] - cur_k;
-                    bt[j] = Batch{cur, cstart[cur] + cur_k, rem < (unsigned)KB ? rem : (unsigned)KB};
-                    cur_k += KB;
-                    any = true;
-                } else {
-                    bt[j] = Batch{-1, 0, 0};
-                }
-            }
-            if (!any) break;
+        Batch bt[G];
+        bool any = next_batches(cstart, ccount, cur, cur_k, bt);
+        Raw raw = load_raw(A, bt[jme], kme);
+        while (any) {
+            const Batch mine = bt[jme];
+            const int cx = bx * BC + (mine.ci & 3), cy = by * BC + ((mine.ci >> 2) & 3),
+                      cz = bz * BC + (mine.ci >> 4);
+            float W[8], s[9];
+            prepare(A, raw, cx, cy, cz, half == 0, W, s);
 
-            float d[2][8];  // this thread's rows of up to two batches
+            float d[2][8];   // this thread's rows of up to two batches
             int dj[2] = {-1, -1};
+            Batch nbt[G];
+            bool nany;
             if constexpr (MODE != SIMT) {
-                // ---- build A = [W S^ij] and B = W^T in the core-matrix layout ----
                 using O = Op<MODE>;
-                const int unit = tid % (G * O::KG);
-                const int part = tid / (G * O::KG);
-                const int j = unit / O::KG, kg = unit % O::KG;
-                const Batch b = bt[j];
-                const int cx = bx * BC + (b.ci & 3), cy = by * BC + ((b.ci >> 2) & 3),
-                          cz = bz * BC + (b.ci >> 4);
-                float fx[O::EPC], fy[O::EPC], fz[O::EPC], s[O::EPC][9];
-                bool live[O::EPC];
+                // ---- this particle's column of A = [W S^ij] and B = W^T (128-byte swizzle) ----
+                {
+                    unsigned char *Aj = stage + jme * O::BATCH;
+                    unsigned char *Bj = Aj + O::A_BYTES;
+                    const int katom = (kme * O::EB) >> 7;               // which 128-byte K-atom
+                    const int kin = (kme * O::EB) & 127;                // byte inside the row
+                    const int chunk = kin >> 4, inb = kin & 15;
+                    unsigned char *abase = Aj + katom * O::A_KSTRIDE + inb;
+                    unsigned char *bbase = Bj + katom * 1024 + inb;
 #pragma unroll
-                for (int e = 0; e < O::EPC; ++e)
-                    live[e] = load_particle(A, b, kg * O::EPC + e, cx, cy, cz, part == 0, fx[e],
-                                            fy[e], fz[e], s[e]);
-                unsigned char *Aj = stage + j * O::BATCH;
-                unsigned char *Bj = Aj + O::A_BYTES;
+                    for (int a = 0; a < 8; ++a) {
+                        const int off = a * 128 + ((chunk ^ a) << 4);
 #pragma unroll
-                for (int c = 0; c < 9; ++c) {
-                    if (c % O::PARTS != part) continue;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int a = (i + kg) & 7;  // rotated row order: conflict-free phases
-                        float v[O::EPC];
-#pragma unroll
-                        for (int e = 0; e < O::EPC; ++e)
-                            v[e] = live[e] ? s[e][c] * corner_w(a, fx[e], fy[e], fz[e]) : 0.f;
-                        unsigned char *dst = Aj + c * O::SBO + kg * 128 + a * 16;
-                        if (MODE == TF32) {
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(
-                                tc::to_tf32(v[0]), tc::to_tf32(v[1]), tc::to_tf32(v[2]), tc::to_tf32(v[3]));
-                        } else {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                __nv_bfloat162 t2 = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
-                                pk[h] = *reinterpret_cast<uint32_t *>(&t2);
-                            }
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        for (int c = 0; c < 9; ++c) {
+                            if ((c < 5) != (half == 0)) continue;
+                            const float v = s[c] * W[a];
+                            unsigned char *dst = abase + c * 1024 + off;
+                            if (MODE == TF32) *reinterpret_cast<uint32_t *>(dst) = tc::to_tf32(v);
+                            else *reinterpret_cast<__nv_bfloat16 *>(dst) = __float2bfloat16_rn(v);
                         }
-                    }
-                }
-                if (part == O::PARTS - 1) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int nn = (i + kg) & 7;
-                        float v[O::EPC];
-#pragma unroll
-                        for (int e = 0; e < O::EPC; ++e)
-                            v[e] = live[e] ? corner_w(nn, fx[e], fy[e], fz[e]) : 0.f;
-                        unsigned char *dst = Bj + kg * 128 + nn * 16;
-                        if (MODE == TF32) {
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(
-                                tc::to_tf32(v[0]), tc::to_tf32(v[1]), tc::to_tf32(v[2]), tc::to_tf32(v[3]));
-                        } else {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                __nv_bfloat162 t2 = __floats2bfloat162_rn(v[2 * h], v[2 * h + 1]);
-                                pk[h] = *reinterpret_cast<uint32_t *>(&t2);
-                            }
-                            *reinterpret_cast<uint4 *>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        if (half == 0) {
+                            unsigned char *dstb = bbase + off;
+                            if (MODE == TF32) *reinterpret_cast<uint32_t *>(dstb) = tc::to_tf32(W[a]);
+                            else *reinterpret_cast<__nv_bfloat16 *>(dstb) = __float2bfloat16_rn(W[a]);
                         }
                     }
                 }
@@ -302,20 +337,31 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                 if (tid == 0) {
                     tc::fence_after_sync();
                     constexpr uint32_t idesc = tc::instr_desc(MODE == TF32 ? 2u : 1u, 128, 16);
+                    const uint64_t ad0 = tc::smem_desc_sw128(tc::smem_addr(stage), 1024);
+                    const uint64_t bd0 = tc::smem_desc_sw128(tc::smem_addr(stage + O::A_BYTES), 1024);
+                    // batch-major: consecutive instructions chain on one accumulator
+                    // (measured faster than interleaving the G accumulators)
+#pragma unroll
                     for (int jj = 0; jj < G; ++jj) {
                         if (bt[jj].ci < 0) continue;
-                        const uint32_t a0 = tc::smem_addr(stage + jj * O::BATCH);
-                        const uint32_t b0 = a0 + O::A_BYTES;
+                        const uint64_t joff = (uint64_t)(jj * O::BATCH) >> 4;  // descriptor units
 #pragma unroll
                         for (int ks = 0; ks < O::KSTEPS; ++ks) {
-                            const uint64_t ad = tc::smem_desc(a0 + ks * 256, 128, O::SBO);
-                            const uint64_t bd = tc::smem_desc(b0 + ks * 256, 128, O::SBO);
-                            tc::mma<MODE == TF32>(tmem + 16 * jj, ad, bd, idesc, ks > 0);
+                            // 32 bytes of K per instruction: K-atom ks*32/128, offset inside it
+                            const uint32_t kb = ks * 32;
+                            const uint32_t ka = (kb >> 7), ko = kb & 127;
+                            const uint64_t aoff = (ka * O::A_KSTRIDE + ko) >> 4;
+                            const uint64_t boff = (ka * 1024 + ko) >> 4;
+                            tc::mma<MODE == TF32>(tmem + 16 * jj, ad0 + joff + aoff, bd0 + joff + boff,
+                                                  idesc, ks > 0);
                         }
                     }
                     tc::commit(mbar);
                 }
-                // bounded wait; the verdict is made uniform across the CTA
+                // the next group's particles load while the tensor core works
+                nany = next_batches(cstart, ccount, cur, cur_k, nbt);
+                raw = load_raw(A, nbt[jme], kme);
+
                 const bool late = __syncthreads_or(!tc::mbar_wait(mbar, phase, kMaxPolls));
                 if (late) {
                     timed_out = true;
@@ -327,39 +373,30 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
 
                 // ---- read the accumulators back: warp quadrant q holds rows 32q..32q+31 ----
                 const int q = warp & 3;
-                if (q < 3) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int jj = (warp >> 2) + 2 * h;
-                        if (bt[jj].ci < 0) continue;  // warp-uniform
-                        tc::tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + 16 * jj, d[h]);
-                        dj[h] = jj;
-                    }
+                const int jj = warp >> 2;  // one batch per warp: warps 4j..4j+3 cover its 128 lanes
+                if (q < 3 && bt[jj].ci >= 0) {  // warp-uniform
+                    tc::tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + 16 * jj, d[0]);
+                    dj[0] = jj;
                 }
                 tc::fence_before_sync();
             } else {
                 // ---- CUDA-core baseline: per-particle W and s staged in shared memory ----
                 float *ps = reinterpret_cast<float *>(stage);  // [G][KB][17]
-                for (int u = tid; u < G * KB; u += kThreads) {
-                    const int j = u / KB, k = u % KB;
-                    const Batch b = bt[j];
-                    const int cx = bx * BC + (b.ci & 3), cy = by * BC + ((b.ci >> 2) & 3),
-                              cz = bz * BC + (b.ci >> 4);
-                    float fx = 0.f, fy = 0.f, fz = 0.f, s[9];
-                    const bool live = load_particle(A, b, k, cx, cy, cz, true, fx, fy, fz, s);
-                    float *dst = ps + (size_t)u * 17;
+                if (half == 0) {
+                    float *dst = ps + (size_t)pme * 17;
 #pragma unroll
-                    for (int a = 0; a < 8; ++a) dst[a] = live ? corner_w(a, fx, fy, fz) : 0.f;
+                    for (int a = 0; a < 8; ++a) dst[a] = W[a];
 #pragma unroll
-                    for (int c = 0; c < 9; ++c) dst[8 + c] = live ? s[c] : 0.f;
+                    for (int c = 0; c < 9; ++c) dst[8 + c] = s[c];
                 }
+                nany = next_batches(cstart, ccount, cur, cur_k, nbt);
+                raw = load_raw(A, nbt[jme], kme);
                 __syncthreads();
-                // thread -> (batch, row); rows 0..71 of batches {warp>>2, warp>>2 + 2}
                 const int q = warp & 3;
                 const int r = 32 * q + lane;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int jj = (warp >> 2) + 2 * h;
+                for (int h = 0; h < 1; ++h) {
+                    const int jj = warp >> 2;
                     if (q >= 3 || bt[jj].ci < 0) continue;
                     dj[h] = jj;
 #pragma unroll
@@ -387,7 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                         const int ci = bt[dj[h]].ci;
                         const int nx = (ci & 3) + (a & 1), ny = ((ci >> 2) & 3) + ((a >> 1) & 1),
                                   nz = (ci >> 4) + (a >> 2);
-                        float *row = acc + ((nz * WN + ny) * WN + nx) * 243 + c;
+                        const int wr = nz * WN + ny;
+                        float *row = acc + wr * ACC_ROW + rsh[wr] + nx * 243 + c;
 #pragma unroll
                         for (int nn = 0; nn < 8; ++nn) {
                             const int o = ((nn >> 2) - (a >> 2) + 1) * 9 +
@@ -398,43 +436,57 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                     }
                 }
             }
-            __syncthreads();  // staging, TMEM slots and the batch cursor are reused
+            __syncthreads();  // staging, TMEM slots and the batch list are reused
             if (MODE != SIMT) tc::fence_after_sync();
+#pragma unroll
+            for (int j = 0; j < G; ++j) bt[j] = nbt[j];
+            any = nany;
         }
 
-        // ---- flush the node window: contiguous x-runs of node blocks, vector reductions ----
+        // ---- flush the node window: each row of 5 node blocks is contiguous in M ----
+        tc::fence_proxy_async_smem();  // the window's shared-memory reductions, for the TMA
         __syncthreads();
         for (int row = 0; row < WN * WN; ++row) {
-            const int ny = row % WN, nz = row / WN;
-            const int gy = (by * BC + ny) % A.N[1];
-            const int gz = (bz * BC + nz) % A.N[2];
+            const int gy = (by * BC + row % WN) % A.N[1];
+            const int gz = (bz * BC + row / WN) % A.N[2];
+            const float *src = acc + row * ACC_ROW + rsh[row];
             int nx0 = 0;
             while (nx0 < WN) {
                 const int gx0 = (bx * BC + nx0) % A.N[0];
                 int len = WN - nx0;
-                if (gx0 + len > A.N[0]) len = A.N[0] - gx0;
-                const long long g0 = (((long long)gz * A.N[1] + gy) * A.N[0] + gx0) * 243;
-                const float *src = acc + (row * WN + nx0) * 243;
+                if (gx0 + len > A.N[0]) len = A.N[0] - gx0;  // the row wraps at the x boundary
+                float *dst = A.M + (((long long)gz * A.N[1] + gy) * A.N[0] + gx0) * 243;
+                const float *sp = src + nx0 * 243;
                 const int L = len * 243;
-                const int head = (int)((4 - (g0 & 3)) & 3) < L ? (int)((4 - (g0 & 3)) & 3) : L;
-                const int nvec = (L - head) / 4;
-                for (int i = tid; i < head; i += kThreads)
-                    if (src[i] != 0.f) red_add_f32(A.M + g0 + i, src[i]);
-                for (int i = tid; i < nvec; i += kThreads) {
-                    const float *sv = src + head + 4 * i;
-                    const float v0 = sv[0], v1 = sv[1], v2 = sv[2], v3 = sv[3];
-                    if (v0 != 0.f || v1 != 0.f || v2 != 0.f || v3 != 0.f)
-                        red_add_v4_f32(A.M + g0 + head + 4 * i, v0, v1, v2, v3);
+                const int head = min((int)((16 - (reinterpret_cast<uintptr_t>(dst) & 15)) & 15) / 4, L);
+                const bool same = ((reinterpret_cast<uintptr_t>(sp + head) & 15) == 0) &&
+                                  ((reinterpret_cast<uintptr_t>(dst + head) & 15) == 0);
+                if (same) {
+                    // aligned body: one bulk reduce-add; head and tail (< 4 floats each) by threads
+                    const int body = (L - head) & ~3;
+                    if (tid == 0 && body > 0)
+                        tc::bulk_reduce_add_f32(dst + head, sp + head, (uint32_t)body * 4);
+                    const int e = tid - 1;  // threads 1..7
+                    if (e >= 0 && e < head) red_add_f32(dst + e, sp[e]);
+                    const int t = head + body + (e - 3);
+                    if (e >= 3 && e < 7 && t < L) red_add_f32(dst + t, sp[t]);
+                } else {
+                    // the part after a wrap: shared and global alignment differ
+                    for (int i = tid; i < L; i += kThreads)
+                        if (sp[i] != 0.f) red_add_f32(dst + i, sp[i]);
                 }
-                for (int i = head + 4 * nvec + tid; i < L; i += kThreads)
-                    if (src[i] != 0.f) red_add_f32(A.M + g0 + i, src[i]);
                 nx0 += len;
             }
+        }
+        if (tid == 0) {
+            tc::bulk_commit();
+            tc::bulk_wait_read_all();  // the window may be cleared once the TMA has read it
         }
         __syncthreads();
         for (int i = tid; i < ACC_FLOATS; i += kThreads) acc[i] = 0.f;
     }
 
+    if (tid == 0) tc::bulk_wait_all();
     if (MODE != SIMT) {
         // after a timeout, give the outstanding MMAs one more bounded wait
         if (timed_out) (void)tc::mbar_wait(mbar, phase, kMaxPolls);
@@ -449,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
 
 template <int MODE>
 size_t smem_bytes() {
-    return ACC_BYTES + Op<MODE>::STAGING + 64 * 8 + 16;
+    return Op<MODE>::STAGING + ACC_BYTES + 64 * 8 + 32 * 4 + 16;
 }
 
 template <int MODE>

@@ -28,6 +28,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
     return d;
 }
 
+// 64-bit shared-memory descriptor for a K-major operand in the 128-byte swizzled
+// layout: 8-row atoms of 8 x 128 bytes (1024 bytes, 1024-byte aligned), the 16-byte
+// chunk c of row r stored at chunk c ^ (r % 8); SBO = distance between 8-row atoms.
+// One MMA reads 32 bytes of K from each row, starting `saddr` bytes into the atom.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;  // leading byte offset: unused for swizzled K-major operands
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;  // layout type: 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor for kind::tf32 / kind::f16: D fp32, A and B K-major.
 // fmt: 1 = BF16 (kind::f16), 2 = TF32 (kind::tf32).
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t fmt, uint32_t M, uint32_t N) {
@@ -105,6 +119,28 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- bulk asynchronous copies (TMA engine, no tensor map) ------------------
+// dst[0..bytes) += src[0..bytes) element-wise in fp32, global <- shared; both
+// addresses 16-byte aligned, bytes a multiple of 16.  Completion is tracked by
+// the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const float *ssrc, uint32_t bytes) {
+    asm volatile(
+        "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+        "r"(smem_addr(ssrc)), "r"(bytes)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the committed bulk groups have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until the committed bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---- mbarrier -------------------------------------------------------------
