@@ -61,6 +61,8 @@ typedef struct pcg_stats {
 
 #define PCG_FLAG_BAD_LAYOUT 1u /* tile_offsets / cell_offsets not monotone or out of range */
 #define PCG_FLAG_CELL_MISMATCH 2u /* mass matrix: a particle not inside the cell it is listed under */
+#define PCG_FLAG_TIMEOUT 4u       /* a bounded wait for an asynchronous copy or a tensor-core result
+                                     gave up; the call's output is invalid */
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 PCG_API int pcg_version(void);

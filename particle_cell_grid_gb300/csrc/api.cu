@@ -21,7 +21,7 @@ pcg_status zero_f32(float *p, size_t count, cudaStream_t s) {
     if (count == 0) return PCG_OK;
     size_t vec = count / 4 + 1;
     size_t blocks = (vec + 255) / 256;
-    size_t cap = (size_t)kNumSMs * 8;
+    size_t cap = (size_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     prof::Mark mk("zero_f32", s);

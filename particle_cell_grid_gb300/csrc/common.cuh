@@ -11,7 +11,26 @@
 
 namespace pcg {
 
-constexpr int kNumSMs = 152;  // GB300: 2 dies x 76 SMs; grids are sized in multiples of it
+// SMs of the current device (152 on a full GB300: 2 dies x 76), cached per
+// device; grids are sized in multiples of it and persistent grids equal it.
+inline int num_sms() {
+    constexpr int kMaxDev = 64;
+    static int cache[kMaxDev] = {0};  // benign race: every writer stores the same value
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        (void)cudaGetLastError();
+        return 152;
+    }
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+            (void)cudaGetLastError();
+            v = 152;
+        }
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256)
 // Particles per CTA of the tiled kernel: a power of two in [1024, 16384], about
 // 16 chunks per SM so that the last wave is short.
 long long chunk_for(long long n) {
-    long long target = n / ((long long)kNumSMs * 16);
+    long long target = n / ((long long)num_sms() * 16);
     long long c = 1024;
     while (c < target && c < 16384) c <<= 1;
     return c;
@@ -143,7 +143,7 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
         size_t work = nJ / 4 > (size_t)nchunks ? nJ / 4 : (size_t)nchunks;
         if (tiled && (size_t)g.n_tiles > work) work = g.n_tiles;
         size_t blocks = (work + 255) / 256;
-        const size_t cap = (size_t)kNumSMs * 8;
+        const size_t cap = (size_t)num_sms() * 8;
         if (blocks > cap) blocks = cap;
         if (blocks < 1) blocks = 1;
         prof::Mark mk("deposit_prep", s);
@@ -155,7 +155,7 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
     if (n == 0) return PCG_OK;
     if (!tiled) {
         const long long want = (n + 255) / 256;
-        const long long cap = (long long)kNumSMs * 16;
+        const long long cap = (long long)num_sms() * 16;
         const unsigned blocks = (unsigned)(want < cap ? want : cap);
         prof::Mark mk("deposit_flat", s);
         if (dim == 2) {

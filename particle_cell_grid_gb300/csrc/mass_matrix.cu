@@ -54,7 +54,6 @@ constexpr int ACC_FLOATS = WN * WN * ACC_ROW;
 constexpr int ACC_BYTES = (ACC_FLOATS * 4 + 1023) / 1024 * 1024;
 constexpr uint32_t kTmemCols = 64;  // G accumulators of 16 columns
 constexpr uint32_t kMaxPolls = 1u << 22;
-constexpr unsigned kFlagTimeout = 4u;
 
 enum Mode { TF32 = 0, BF16 = 1, SIMT = 2 };
 
@@ -365,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                 const bool late = __syncthreads_or(!tc::mbar_wait(mbar, phase, kMaxPolls));
                 if (late) {
                     timed_out = true;
-                    if (tid == 0 && A.flags) atomicOr(A.flags, kFlagTimeout);
+                    if (tid == 0 && A.flags) atomicOr(A.flags, PCG_FLAG_TIMEOUT);
                     break;
                 }
                 phase ^= 1;
@@ -510,7 +509,7 @@ pcg_status launch(const Args &A, cudaStream_t s) {
     PCG_CHECK_CUDA(cudaFuncSetAttribute(mass_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)smem));
     const long long nblocks = (long long)A.nb[0] * A.nb[1] * A.nb[2];
-    const long long grid = nblocks < kNumSMs ? nblocks : kNumSMs;
+    const long long grid = nblocks < num_sms() ? nblocks : num_sms();
     prof::Mark mk(MODE == TF32 ? "mass_matrix_tf32" : MODE == BF16 ? "mass_matrix_bf16" : "mass_matrix_simt", s);
     mass_kernel<MODE><<<(unsigned)grid, kThreads, smem, s>>>(A);
     return launch_status();
