@@ -731,6 +731,335 @@ __global__ void __launch_bounds__(512, MINB)
     warp_add_u64(ctr.n_invalid, n_inv);
 }
 
+// ---------------------------------------------------------------------------
+// 3D CIC with 8^3 tiles, persistent: one CTA of 512 threads per SM walks the
+// chunks b, b + grid, ... of the tile-sorted array in rounds of 4096
+// particles (8 per thread, loaded as float4 per field).  One thread per cell of
+// the tile keeps the cell's 8 corners x 3 components in registers for the
+// whole tile segment.  A round is distributed to the cells through a
+// transposed staging array of float2 pairs, st[pair][rank][cell]: the placing
+// atomic returns the rank, and a warp's 32 cells read rank r from 32
+// consecutive 8-byte words (conflict-free).  With 8 particles per cell per
+// round on average, a warp's longest cell list is ~1.5x the mean (a round of
+// 1024 would leave two thirds of the lanes idle).  A cell holds up to CAP
+// particles per round; further ones, and particles that drifted into the halo,
+// go to a short list deposited with per-particle shared reductions.
+// The next round's particles are loaded into registers before this round is
+// accumulated, so their latency hides behind the accumulation.
+// ---------------------------------------------------------------------------
+template <int HALO>
+struct Cic5Cfg {
+    static constexpr int THREADS = 512;
+    static constexpr int PPT = 8;               // particles per thread per round
+    static constexpr int R = THREADS * PPT;     // round size
+    static constexpr int CAP = 12;              // staged particles per cell and round
+    static constexpr int HCAP = 512;            // listed halo / overflow particles per round
+    using C = TileCfg<3, 1, 8, HALO>;
+    static constexpr int NK = C::NKEYS;         // cells of the tile (one thread each)
+    static_assert(NK <= THREADS, "one thread per grouped cell");
+    static constexpr size_t SMEM = (size_t)C::FLOATS * 4 + (size_t)3 * CAP * NK * 8 +
+                                   (size_t)7 * HCAP * 4 + (size_t)NK * 4;
+};
+
+// Position of a CTA in its work: chunk, tile segment (tile t, valid particles
+// [lo, hi)) and round base rb (a multiple of 4).
+struct RoundPos {
+    long long c;      // chunk
+    long long rb;     // round base
+    long long lo, hi; // tile segment inside the chunk
+    unsigned t;       // tile (n_tiles: the invalid tail; > n_tiles: no more work)
+};
+
+__device__ __forceinline__ bool seg_of_tile(const Geom &g, const uint32_t *__restrict__ offs, long long n,
+                                            long long c0, long long c1, unsigned t, RoundPos &r) {
+    long long s = (long long)offs[t];
+    if (s < c0) s = c0;
+    long long e = (t < g.n_tiles) ? (long long)offs[t + 1] : c1;
+    if (e > c1) e = c1;
+    r.t = t;
+    r.lo = s;
+    r.hi = e;
+    r.rb = s & ~3ll;
+    return s < c1;  // false: the tile starts after the chunk
+}
+
+// First non-empty tile segment at or after tile t of chunk c, or the next chunk's.
+__device__ __forceinline__ void seek(const Geom &g, const uint32_t *__restrict__ offs,
+                                     const unsigned *__restrict__ chunk_tile, long long n, long long chunk,
+                                     long long nchunks, long long c, unsigned t, RoundPos &r) {
+    for (; c < nchunks; c += gridDim.x, t = 0xffffffffu) {
+        const long long c0 = c * chunk, c1 = min(n, c0 + chunk);
+        if (t == 0xffffffffu) t = min(chunk_tile[c], g.n_tiles);
+        r.c = c;
+        for (; t <= g.n_tiles; ++t) {
+            if (!seg_of_tile(g, offs, n, c0, c1, t, r)) break;
+            if (r.hi > r.lo) return;
+            if (t == g.n_tiles) break;
+        }
+    }
+    r.c = nchunks;
+    r.t = g.n_tiles + 1;
+}
+
+template <int HALO>
+__global__ void __launch_bounds__(512, 1)
+    deposit_cic3d_v5_kernel(Geom g, Particles P, long long n, const uint32_t *__restrict__ offs,
+                            const unsigned *__restrict__ chunk_tile, long long chunk, long long nchunks,
+                            float *__restrict__ J, Counters ctr, bool vec) {
+    using K = Cic5Cfg<HALO>;
+    using C = typename K::C;
+    constexpr int NK = K::NK, CAP = K::CAP, HCAP = K::HCAP;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    float *scratch = reinterpret_cast<float *>(dsm);                          // [3][CELLS]
+    float2 *st = reinterpret_cast<float2 *>(scratch + C::FLOATS);             // [3][CAP][NK]
+    float *hbuf = reinterpret_cast<float *>(st + 3 * CAP * NK);               // [7][HCAP]
+    unsigned *cnt = reinterpret_cast<unsigned *>(hbuf + 7 * HCAP);            // [NK]
+    __shared__ unsigned hcount[2];
+
+    const int tid = threadIdx.x;
+    unsigned n_esc = 0, n_inv = 0;
+    const int kx0 = tid % C::KR + C::KLO, ky0 = (tid / C::KR) % C::KR + C::KLO,
+              kz0 = tid / (C::KR * C::KR) + C::KLO;
+
+    for (int i = tid; i < C::FLOATS; i += K::THREADS) scratch[i] = 0.f;
+    if (tid < NK) cnt[tid] = 0;
+    if (tid < 2) hcount[tid] = 0;
+    float acc[8][3];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) acc[a][0] = acc[a][1] = acc[a][2] = 0.f;
+
+    // the particles of one round, this thread's 8 slots
+    float X[8], Y[8], Z[8], VX[8], VY[8], VZ[8], Q[8];
+    auto load_round = [&](const RoundPos &r) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long b = r.rb + h * (K::R / 2) + 4 * tid;
+            if (vec && b + 3 < n) {
+                const float4 a = *reinterpret_cast<const float4 *>(P.x + b);
+                const float4 bb = *reinterpret_cast<const float4 *>(P.y + b);
+                const float4 c = *reinterpret_cast<const float4 *>(P.z + b);
+                const float4 d = *reinterpret_cast<const float4 *>(P.vx + b);
+                const float4 e = *reinterpret_cast<const float4 *>(P.vy + b);
+                const float4 f = *reinterpret_cast<const float4 *>(P.vz + b);
+                const float4 q = *reinterpret_cast<const float4 *>(P.q + b);
+                X[4 * h] = a.x; X[4 * h + 1] = a.y; X[4 * h + 2] = a.z; X[4 * h + 3] = a.w;
+                Y[4 * h] = bb.x; Y[4 * h + 1] = bb.y; Y[4 * h + 2] = bb.z; Y[4 * h + 3] = bb.w;
+                Z[4 * h] = c.x; Z[4 * h + 1] = c.y; Z[4 * h + 2] = c.z; Z[4 * h + 3] = c.w;
+                VX[4 * h] = d.x; VX[4 * h + 1] = d.y; VX[4 * h + 2] = d.z; VX[4 * h + 3] = d.w;
+                VY[4 * h] = e.x; VY[4 * h + 1] = e.y; VY[4 * h + 2] = e.z; VY[4 * h + 3] = e.w;
+                VZ[4 * h] = f.x; VZ[4 * h + 1] = f.y; VZ[4 * h + 2] = f.z; VZ[4 * h + 3] = f.w;
+                Q[4 * h] = q.x; Q[4 * h + 1] = q.y; Q[4 * h + 2] = q.z; Q[4 * h + 3] = q.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const long long p = (b + j < n) ? b + j : 0;
+                    X[4 * h + j] = P.x[p]; Y[4 * h + j] = P.y[p]; Z[4 * h + j] = P.z[p];
+                    VX[4 * h + j] = P.vx[p]; VY[4 * h + j] = P.vy[p]; VZ[4 * h + j] = P.vz[p];
+                    Q[4 * h + j] = P.q[p];
+                }
+            }
+        }
+    };
+
+    RoundPos cur;
+    seek(g, offs, chunk_tile, n, chunk, nchunks, blockIdx.x, 0xffffffffu, cur);
+    // the invalid tail and empty work never enter the round loop
+    auto tail = [&](const RoundPos &r) {
+        for (long long p = r.lo + tid; p < r.hi; p += K::THREADS) {
+            const float x = P.x[p], y = P.y[p], z = P.z[p];
+            if (!in_domain<3>(g, x, y, z)) {
+                ++n_inv;
+                continue;
+            }
+            const float q = P.q[p];
+            deposit_global<3, 1>(g, J, x, y, z, q * P.vx[p], q * P.vy[p], q * P.vz[p]);
+        }
+    };
+    while (cur.t == g.n_tiles) {  // a chunk that holds only invalid-tail particles
+        tail(cur);
+        seek(g, offs, chunk_tile, n, chunk, nchunks, cur.c + gridDim.x, 0xffffffffu, cur);
+    }
+    if (cur.t > g.n_tiles) {
+        warp_add_u64(ctr.n_invalid, n_inv);
+        return;
+    }
+    load_round(cur);
+    __syncthreads();  // scratch, counters zeroed
+    int parity = 0;
+    while (true) {
+        // ---- place the round held in registers (tile cur.t, origin o*) ----
+        const int tx = (int)(cur.t % (unsigned)g.nt[0]);
+        const int ty = (int)((cur.t / (unsigned)g.nt[0]) % (unsigned)g.nt[1]);
+        const int tz = (int)(cur.t / ((unsigned)g.nt[0] * (unsigned)g.nt[1]));
+        const int ox = tx * 8, oy = ty * 8, oz = tz * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const long long p = cur.rb + (j >> 2) * (K::R / 2) + 4 * tid + (j & 3);
+            if (p < cur.lo || p >= cur.hi) continue;
+            const float x = X[j], y = Y[j], z = Z[j];
+            if (!in_domain<3>(g, x, y, z)) {
+                ++n_inv;
+                continue;
+            }
+            const float qq = Q[j];
+            const float qvx = qq * VX[j], qvy = qq * VY[j], qvz = qq * VZ[j];
+            float fx_, fy_, fz_;
+            const int fx = first_node<1>(x, fx_);
+            const int fy = first_node<1>(y, fy_);
+            const int fz = first_node<1>(z, fz_);
+            const int lx = local_index<2, 8, HALO>(fx, ox, g.N[0]);
+            const int ly = local_index<2, 8, HALO>(fy, oy, g.N[1]);
+            const int lz = local_index<2, 8, HALO>(fz, oz, g.N[2]);
+            const bool home = (lx >= C::KLO) & (lx < C::KHI) & (ly >= C::KLO) & (ly < C::KHI) &
+                              (lz >= C::KLO) & (lz < C::KHI);
+            if (home) {
+                const int k = ((lz - C::KLO) * C::KR + (ly - C::KLO)) * C::KR + (lx - C::KLO);
+                const unsigned r = atomicAdd(&cnt[k], 1u);
+                if (r < (unsigned)CAP) {
+                    float2 *dst = st + r * NK + k;
+                    dst[0] = make_float2(fx_, fy_);
+                    dst[CAP * NK] = make_float2(fz_, qvx);
+                    dst[2 * CAP * NK] = make_float2(qvy, qvz);
+                    continue;
+                }
+                // more than CAP in this cell: listed below like a halo particle
+            } else {
+                const bool fits = (lx >= -HALO) & (lx + 1 < 8 + HALO) & (ly >= -HALO) & (ly + 1 < 8 + HALO) &
+                                  (lz >= -HALO) & (lz + 1 < 8 + HALO);
+                if (!fits) {
+                    ++n_esc;
+                    deposit_global<3, 1>(g, J, x, y, z, qvx, qvy, qvz);
+                    continue;
+                }
+            }
+            const unsigned hs = atomicAdd(&hcount[parity], 1u);
+            if (hs < (unsigned)HCAP) {
+                hbuf[0 * HCAP + hs] = fx_;
+                hbuf[1 * HCAP + hs] = fy_;
+                hbuf[2 * HCAP + hs] = fz_;
+                hbuf[3 * HCAP + hs] = qvx;
+                hbuf[4 * HCAP + hs] = qvy;
+                hbuf[5 * HCAP + hs] = qvz;
+                hbuf[6 * HCAP + hs] = __int_as_float(((lx + HALO) & 255) | (((ly + HALO) & 255) << 8) |
+                                                     (((lz + HALO) & 255) << 16));
+            } else {
+                scratch_particle<3, 1, 8, HALO>(scratch, lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
+            }
+        }
+        // ---- the next round: position, and its particles into registers ----
+        RoundPos nxt = cur;
+        nxt.rb = cur.rb + K::R;
+        if (nxt.rb >= cur.hi) seek(g, offs, chunk_tile, n, chunk, nchunks, cur.c, cur.t + 1, nxt);
+        const bool tile_ends = nxt.t != cur.t || nxt.c != cur.c;
+        const bool more = nxt.t < g.n_tiles;
+        __syncthreads();  // the round is staged
+        if (more) load_round(nxt);
+
+        // ---- every cell's thread adds its staged particles in registers ----
+        if (tid == 0) hcount[parity ^ 1] = 0;  // the list the next round fills
+        if (tid < NK) {
+            const unsigned m0 = cnt[tid];
+            const unsigned m = m0 < (unsigned)CAP ? m0 : (unsigned)CAP;
+            cnt[tid] = 0;
+            for (unsigned r = 0; r < m; ++r) {
+                const float2 a = st[r * NK + tid];
+                const float2 b = st[CAP * NK + r * NK + tid];
+                const float2 c = st[2 * CAP * NK + r * NK + tid];
+                const float wx[2] = {1.f - a.x, a.x}, wy[2] = {1.f - a.y, a.y}, wz[2] = {1.f - b.x, b.x};
+#pragma unroll
+                for (int kz = 0; kz < 2; ++kz)
+#pragma unroll
+                    for (int ky = 0; ky < 2; ++ky) {
+                        const float wyz = wy[ky] * wz[kz];
+#pragma unroll
+                        for (int kx = 0; kx < 2; ++kx) {
+                            const float W = wyz * wx[kx];
+                            float *ac = acc[(kz * 2 + ky) * 2 + kx];
+                            ac[0] = fmaf(b.y, W, ac[0]);
+                            ac[1] = fmaf(c.x, W, ac[1]);
+                            ac[2] = fmaf(c.y, W, ac[2]);
+                        }
+                    }
+            }
+        }
+        {
+            const unsigned nh = min(hcount[parity], (unsigned)HCAP);
+            for (unsigned h = tid; h < nh; h += K::THREADS) {
+                const int pk = __float_as_int(hbuf[6 * HCAP + h]);
+                scratch_particle<3, 1, 8, HALO>(scratch, (pk & 255) - HALO, ((pk >> 8) & 255) - HALO,
+                                                ((pk >> 16) & 255) - HALO, hbuf[h], hbuf[HCAP + h],
+                                                hbuf[2 * HCAP + h], hbuf[3 * HCAP + h], hbuf[4 * HCAP + h],
+                                                hbuf[5 * HCAP + h]);
+            }
+        }
+        parity ^= 1;
+        if (tile_ends) {
+            // each cell's corners into the scratch tile once, then one flush
+            if (tid < NK) {
+            const int base = ((kz0 + HALO) * C::TE + (ky0 + HALO)) * C::TE + (kx0 + HALO);
+#pragma unroll
+            for (int kz = 0; kz < 2; ++kz)
+#pragma unroll
+                for (int ky = 0; ky < 2; ++ky) {
+                    float *row = scratch + base + (kz * C::TE + ky) * C::TE;
+#pragma unroll
+                    for (int kx = 0; kx < 2; ++kx) {
+                        float *ac = acc[(kz * 2 + ky) * 2 + kx];
+                        red_shared_add_f32(row + kx, ac[0]);
+                        red_shared_add_f32(row + C::CELLS + kx, ac[1]);
+                        red_shared_add_f32(row + 2 * C::CELLS + kx, ac[2]);
+                        ac[0] = ac[1] = ac[2] = 0.f;
+                    }
+                }
+            }
+            __syncthreads();
+            flush_scratch<3, 8, HALO, K::THREADS>(g, scratch, J, ox, oy, oz);
+            __syncthreads();
+            for (int i = tid; i < C::FLOATS; i += K::THREADS) scratch[i] = 0.f;
+        }
+        if (!more) {
+            if (nxt.t == g.n_tiles) {  // the invalid tail of this chunk, then whatever follows
+                RoundPos r = nxt;
+                while (r.t == g.n_tiles) {
+                    tail(r);
+                    seek(g, offs, chunk_tile, n, chunk, nchunks, r.c + gridDim.x, 0xffffffffu, r);
+                }
+                if (r.t < g.n_tiles) {
+                    // more tiles after an invalid tail: continue with them
+                    __syncthreads();
+                    cur = r;
+                    load_round(cur);
+                    __syncthreads();
+                    continue;
+                }
+            }
+            break;
+        }
+        cur = nxt;
+        __syncthreads();  // staging read, scratch flushed and zeroed
+    }
+    warp_add_u64(ctr.n_escaped, n_esc);
+    warp_add_u64(ctr.n_invalid, n_inv);
+}
+
+template <int HALO>
+pcg_status launch_cic3d_v5(const Geom &g, long long n, const Particles &P, const uint32_t *offs, float *J,
+                           const Counters &ctr, const unsigned *chunk_tile, long long chunk, cudaStream_t s) {
+    using K = Cic5Cfg<HALO>;
+    const long long nchunks = (n + chunk - 1) / chunk;
+    if (nchunks == 0) return PCG_OK;
+    const bool vec = aligned16(P.x) && aligned16(P.y) && aligned16(P.z) && aligned16(P.vx) &&
+                     aligned16(P.vy) && aligned16(P.vz) && aligned16(P.q);
+    const long long sms = num_sms();
+    const unsigned grid = (unsigned)(nchunks < sms ? nchunks : sms);
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(deposit_cic3d_v5_kernel<HALO>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K::SMEM));
+    prof::Mark mk("deposit_tiled", s);
+    deposit_cic3d_v5_kernel<HALO><<<grid, K::THREADS, K::SMEM, s>>>(g, P, n, offs, chunk_tile, chunk, nchunks,
+                                                                    J, ctr, vec);
+    return launch_status();
+}
+
 template <int HALO>
 pcg_status launch_cic3d(const Geom &g, long long n, const Particles &P, const uint32_t *offs,
                         float *J, const Counters &ctr, const unsigned *chunk_tile, long long chunk,
@@ -787,7 +1116,7 @@ pcg_status launch_tiled(const Geom &g, long long n, const Particles &P, const ui
                         int block, cudaStream_t s) {
     if constexpr (DIM == 3 && ORDER == 1 && TILE == 8) {
         // block 512 asks for one 512-thread CTA per SM with the full register file
-        return launch_cic3d<HALO>(g, n, P, offs, J, ctr, chunk_tile, chunk, block == 512 ? 1 : 2, s);
+        return launch_cic3d_v5<HALO>(g, n, P, offs, J, ctr, chunk_tile, chunk, s);
     } else {
         if (block == 512)
             return launch_tiled_t<DIM, ORDER, TILE, HALO, 512>(g, n, P, offs, J, ctr, chunk_tile, chunk, s);

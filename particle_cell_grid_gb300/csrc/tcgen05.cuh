@@ -143,31 +143,9 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Global -> shared bulk copy on the TMA engine; completion is counted in bytes
-// on `mbar` (armed with mbar_arrive_expect_tx).  Both addresses 16-byte aligned,
-// bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *mbar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(sdst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_addr(mbar))
-        : "memory");
-}
-
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(mbar)), "r"(count)
-                 : "memory");
-}
-
-// Make mbarrier initialisations visible to the asynchronous proxy (TMA).
-__device__ __forceinline__ void mbar_init_fence() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// One arrival that also announces `bytes` of asynchronous copies to wait for.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *mbar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(mbar)), "r"(bytes)
                  : "memory");
 }
 
