@@ -255,10 +255,16 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
     # algorithmic bytes per launch of the main kernels
     kbytes = 4 * dim * (1 if separate_keys else 0)
     node_bytes = 12 * int(np.prod(grid))
+    nf = dim + 4  # payload fields: positions, three velocity components, q
     alg = {
         "deposit_tiled": n * (4 * (dim + 4)) + node_bytes,
-        "sort_scatter": n * (kbytes + 2 * 4 * (dim + 4)),
+        "sort_scatter": n * (kbytes + 2 * 4 * nf),
         "sort_count": n * 4 * dim,
+        # pass 1 reads key positions and payload, writes payload and the tile key;
+        # pass 2 reads payload and key, writes payload; one pass: in and out once
+        "sort_partition1": n * (kbytes + 4 * nf + 4 * (nf + 1)),
+        "sort_partition2": n * (4 * (nf + 1) + 4 * nf),
+        "sort_partition": n * (kbytes + 2 * 4 * nf),
     }
     kern = {}
     for name, b in alg.items():
