@@ -757,8 +757,8 @@ struct Cic5Cfg {
     using C = TileCfg<3, 1, 8, HALO>;
     static constexpr int NK = C::NKEYS;         // cells of the tile (one thread each)
     static_assert(NK <= THREADS, "one thread per grouped cell");
-    static constexpr size_t SMEM = (size_t)C::FLOATS * 4 + (size_t)3 * CAP * NK * 8 +
-                                   (size_t)7 * HCAP * 4 + (size_t)NK * 4;
+    static_assert(24 <= 6 * CAP, "the corner values fit in the staging array");
+    static constexpr size_t SMEM = (size_t)3 * CAP * NK * 8 + (size_t)7 * HCAP * 4 + (size_t)NK * 4;
 };
 
 // Position of a CTA in its work: chunk, tile segment (tile t, valid particles
@@ -801,6 +801,46 @@ __device__ __forceinline__ void seek(const Geom &g, const uint32_t *__restrict__
     r.t = g.n_tiles + 1;
 }
 
+// Stencil of one CIC particle at local first node (lx, ly, lz) of the tile at
+// (ox, oy, oz) straight into J with global reductions (periodic wrap): the path
+// of halo and overflow particles.  On this GPU a shared-memory float reduction
+// is a long serial read-modify-write (~87 cycles per dependent op against ~6 for
+// an integer shared atomic), while a global reduction is fire-and-forget.
+template <int HALO>
+__device__ __forceinline__ void stencil_to_global(const Geom &g, float *__restrict__ J, int ox, int oy, int oz,
+                                                  int lx, int ly, int lz, float tx, float ty, float tz, float qvx,
+                                                  float qvy, float qvz) {
+    const float wx[2] = {1.f - tx, tx}, wy[2] = {1.f - ty, ty}, wz[2] = {1.f - tz, tz};
+    int gx[2], gy[2], gz[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        gx[k] = ox + lx + k;
+        gy[k] = oy + ly + k;
+        gz[k] = oz + lz + k;
+        while (gx[k] < 0) gx[k] += g.N[0];
+        while (gx[k] >= g.N[0]) gx[k] -= g.N[0];
+        while (gy[k] < 0) gy[k] += g.N[1];
+        while (gy[k] >= g.N[1]) gy[k] -= g.N[1];
+        while (gz[k] < 0) gz[k] += g.N[2];
+        while (gz[k] >= g.N[2]) gz[k] -= g.N[2];
+    }
+#pragma unroll
+    for (int kz = 0; kz < 2; ++kz)
+#pragma unroll
+        for (int ky = 0; ky < 2; ++ky) {
+            const float wyz = wy[ky] * wz[kz];
+            const long long row = ((long long)gz[kz] * g.N[1] + gy[ky]) * g.N[0];
+#pragma unroll
+            for (int kx = 0; kx < 2; ++kx) {
+                const float W = wyz * wx[kx];
+                float *j = J + row + gx[kx];
+                red_add_f32(j, qvx * W);
+                red_add_f32(j + g.ncells, qvy * W);
+                red_add_f32(j + 2 * g.ncells, qvz * W);
+            }
+        }
+}
+
 template <int HALO>
 __global__ void __launch_bounds__(512, 1)
     deposit_cic3d_v5_kernel(Geom g, Particles P, long long n, const uint32_t *__restrict__ offs,
@@ -810,8 +850,7 @@ __global__ void __launch_bounds__(512, 1)
     using C = typename K::C;
     constexpr int NK = K::NK, CAP = K::CAP, HCAP = K::HCAP;
     extern __shared__ __align__(16) unsigned char dsm[];
-    float *scratch = reinterpret_cast<float *>(dsm);                          // [3][CELLS]
-    float2 *st = reinterpret_cast<float2 *>(scratch + C::FLOATS);             // [3][CAP][NK]
+    float2 *st = reinterpret_cast<float2 *>(dsm);                             // [3][CAP][NK]
     float *hbuf = reinterpret_cast<float *>(st + 3 * CAP * NK);               // [7][HCAP]
     unsigned *cnt = reinterpret_cast<unsigned *>(hbuf + 7 * HCAP);            // [NK]
     __shared__ unsigned hcount[2];
@@ -821,7 +860,6 @@ __global__ void __launch_bounds__(512, 1)
     const int kx0 = tid % C::KR + C::KLO, ky0 = (tid / C::KR) % C::KR + C::KLO,
               kz0 = tid / (C::KR * C::KR) + C::KLO;
 
-    for (int i = tid; i < C::FLOATS; i += K::THREADS) scratch[i] = 0.f;
     if (tid < NK) cnt[tid] = 0;
     if (tid < 2) hcount[tid] = 0;
     float acc[8][3];
@@ -884,7 +922,7 @@ __global__ void __launch_bounds__(512, 1)
         return;
     }
     load_round(cur);
-    __syncthreads();  // scratch, counters zeroed
+    __syncthreads();  // counters zeroed
     int parity = 0;
     while (true) {
         // ---- place the round held in registers (tile cur.t, origin o*) ----
@@ -943,7 +981,7 @@ __global__ void __launch_bounds__(512, 1)
                 hbuf[6 * HCAP + hs] = __int_as_float(((lx + HALO) & 255) | (((ly + HALO) & 255) << 8) |
                                                      (((lz + HALO) & 255) << 16));
             } else {
-                scratch_particle<3, 1, 8, HALO>(scratch, lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
+                stencil_to_global<HALO>(g, J, ox, oy, oz, lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
             }
         }
         // ---- the next round: position, and its particles into registers ----
@@ -986,57 +1024,63 @@ __global__ void __launch_bounds__(512, 1)
             const unsigned nh = min(hcount[parity], (unsigned)HCAP);
             for (unsigned h = tid; h < nh; h += K::THREADS) {
                 const int pk = __float_as_int(hbuf[6 * HCAP + h]);
-                scratch_particle<3, 1, 8, HALO>(scratch, (pk & 255) - HALO, ((pk >> 8) & 255) - HALO,
-                                                ((pk >> 16) & 255) - HALO, hbuf[h], hbuf[HCAP + h],
-                                                hbuf[2 * HCAP + h], hbuf[3 * HCAP + h], hbuf[4 * HCAP + h],
-                                                hbuf[5 * HCAP + h]);
+                stencil_to_global<HALO>(g, J, ox, oy, oz, (pk & 255) - HALO, ((pk >> 8) & 255) - HALO,
+                                        ((pk >> 16) & 255) - HALO, hbuf[h], hbuf[HCAP + h], hbuf[2 * HCAP + h],
+                                        hbuf[3 * HCAP + h], hbuf[4 * HCAP + h], hbuf[5 * HCAP + h]);
             }
         }
         parity ^= 1;
         if (tile_ends) {
-            // each cell's corners into the scratch tile once, then one flush
+            // The tile's flush without shared-memory float atomics: every cell's 8
+            // corners x 3 components go to the (now free) staging area with plain
+            // stores; after a barrier one thread per node sums the up to 8 cell
+            // corners that meet there and adds the total to J once.
+            float *corner = reinterpret_cast<float *>(st);  // [24][NK]
+            __syncthreads();  // every cell's staged particles have been read
             if (tid < NK) {
-            const int base = ((kz0 + HALO) * C::TE + (ky0 + HALO)) * C::TE + (kx0 + HALO);
 #pragma unroll
-            for (int kz = 0; kz < 2; ++kz)
+                for (int a = 0; a < 8; ++a)
 #pragma unroll
-                for (int ky = 0; ky < 2; ++ky) {
-                    float *row = scratch + base + (kz * C::TE + ky) * C::TE;
-#pragma unroll
-                    for (int kx = 0; kx < 2; ++kx) {
-                        float *ac = acc[(kz * 2 + ky) * 2 + kx];
-                        red_shared_add_f32(row + kx, ac[0]);
-                        red_shared_add_f32(row + C::CELLS + kx, ac[1]);
-                        red_shared_add_f32(row + 2 * C::CELLS + kx, ac[2]);
-                        ac[0] = ac[1] = ac[2] = 0.f;
+                    for (int comp = 0; comp < 3; ++comp) {
+                        corner[(a * 3 + comp) * NK + tid] = acc[a][comp];
+                        acc[a][comp] = 0.f;
                     }
-                }
             }
             __syncthreads();
-            flush_scratch<3, 8, HALO, K::THREADS>(g, scratch, J, ox, oy, oz);
-            __syncthreads();
-            for (int i = tid; i < C::FLOATS; i += K::THREADS) scratch[i] = 0.f;
+            constexpr int NR = C::KR + 1;
+            for (int nd = tid; nd < NR * NR * NR; nd += K::THREADS) {
+                const int nx = nd % NR, ny = (nd / NR) % NR, nz = nd / (NR * NR);
+                float sum[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    const int cx = nx - (a & 1), cy = ny - ((a >> 1) & 1), cz = nz - (a >> 2);
+                    if (cx < 0 || cx >= C::KR || cy < 0 || cy >= C::KR || cz < 0 || cz >= C::KR) continue;
+                    const int cell = (cz * C::KR + cy) * C::KR + cx;
+#pragma unroll
+                    for (int comp = 0; comp < 3; ++comp) sum[comp] += corner[(a * 3 + comp) * NK + cell];
+                }
+                int gx = ox + C::KLO + nx, gy = oy + C::KLO + ny, gz = oz + C::KLO + nz;
+                while (gx >= g.N[0]) gx -= g.N[0];
+                while (gy >= g.N[1]) gy -= g.N[1];
+                while (gz >= g.N[2]) gz -= g.N[2];
+                const long long node = ((long long)gz * g.N[1] + gy) * g.N[0] + gx;
+#pragma unroll
+                for (int comp = 0; comp < 3; ++comp)
+                    if (sum[comp] != 0.f) red_add_f32(J + comp * g.ncells + node, sum[comp]);
+            }
         }
         if (!more) {
-            if (nxt.t == g.n_tiles) {  // the invalid tail of this chunk, then whatever follows
-                RoundPos r = nxt;
-                while (r.t == g.n_tiles) {
-                    tail(r);
-                    seek(g, offs, chunk_tile, n, chunk, nchunks, r.c + gridDim.x, 0xffffffffu, r);
-                }
-                if (r.t < g.n_tiles) {
-                    // more tiles after an invalid tail: continue with them
-                    __syncthreads();
-                    cur = r;
-                    load_round(cur);
-                    __syncthreads();
-                    continue;
-                }
+            // the invalid tail sits at the end of the array: after it come only
+            // chunks that are all tail or past the end
+            RoundPos r = nxt;
+            while (r.t == g.n_tiles) {
+                tail(r);
+                seek(g, offs, chunk_tile, n, chunk, nchunks, r.c + gridDim.x, 0xffffffffu, r);
             }
             break;
         }
         cur = nxt;
-        __syncthreads();  // staging read, scratch flushed and zeroed
+        __syncthreads();  // staging and corner values read
     }
     warp_add_u64(ctr.n_escaped, n_esc);
     warp_add_u64(ctr.n_invalid, n_inv);
