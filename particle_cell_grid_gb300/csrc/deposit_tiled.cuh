@@ -841,6 +841,19 @@ __device__ __forceinline__ void stencil_to_global(const Geom &g, float *__restri
         }
 }
 
+// Rare paths of the placing loop, kept out of line: inlined into each of its 8
+// unrolled iterations they multiply the loop's code size.
+static __device__ __noinline__ void escape_to_global(const Geom g, float *J, float x, float y, float z, float qvx,
+                                              float qvy, float qvz) {
+    deposit_global<3, 1>(g, J, x, y, z, qvx, qvy, qvz);
+}
+template <int HALO>
+__device__ __noinline__ void list_full_to_global(const Geom g, float *J, int ox, int oy, int oz, int lx, int ly,
+                                                 int lz, float tx, float ty, float tz, float qvx, float qvy,
+                                                 float qvz) {
+    stencil_to_global<HALO>(g, J, ox, oy, oz, lx, ly, lz, tx, ty, tz, qvx, qvy, qvz);
+}
+
 template <int HALO>
 __global__ void __launch_bounds__(512, 1)
     deposit_cic3d_v5_kernel(Geom g, Particles P, long long n, const uint32_t *__restrict__ offs,
@@ -924,27 +937,64 @@ __global__ void __launch_bounds__(512, 1)
     load_round(cur);
     __syncthreads();  // counters zeroed
     int parity = 0;
+    int ox = 0, oy = 0, oz = 0;  // origin of the current tile
+    // a halo particle, or a grouped one beyond CAP: into this round's short list
+    auto to_list = [&](int lx, int ly, int lz, float fx, float fy, float fz, float qvx, float qvy, float qvz) {
+        const unsigned hs = atomicAdd(&hcount[parity], 1u);
+        if (hs < (unsigned)HCAP) {
+            hbuf[0 * HCAP + hs] = fx;
+            hbuf[1 * HCAP + hs] = fy;
+            hbuf[2 * HCAP + hs] = fz;
+            hbuf[3 * HCAP + hs] = qvx;
+            hbuf[4 * HCAP + hs] = qvy;
+            hbuf[5 * HCAP + hs] = qvz;
+            hbuf[6 * HCAP + hs] = __int_as_float(((lx + HALO) & 255) | (((ly + HALO) & 255) << 8) |
+                                                 (((lz + HALO) & 255) << 16));
+        } else {
+            list_full_to_global<HALO>(g, J, ox, oy, oz, lx, ly, lz, fx, fy, fz, qvx, qvy, qvz);
+        }
+    };
     while (true) {
         // ---- place the round held in registers (tile cur.t, origin o*) ----
         const int tx = (int)(cur.t % (unsigned)g.nt[0]);
         const int ty = (int)((cur.t / (unsigned)g.nt[0]) % (unsigned)g.nt[1]);
         const int tz = (int)(cur.t / ((unsigned)g.nt[0] * (unsigned)g.nt[1]));
-        const int ox = tx * 8, oy = ty * 8, oz = tz * 8;
+        ox = tx * 8;
+        oy = ty * 8;
+        oz = tz * 8;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const long long p = cur.rb + (j >> 2) * (K::R / 2) + 4 * tid + (j & 3);
             if (p < cur.lo || p >= cur.hi) continue;
             const float x = X[j], y = Y[j], z = Z[j];
-            if (!in_domain<3>(g, x, y, z)) {
-                ++n_inv;
-                continue;
-            }
             const float qq = Q[j];
             const float qvx = qq * VX[j], qvy = qq * VY[j], qvz = qq * VZ[j];
             float fx_, fy_, fz_;
             const int fx = first_node<1>(x, fx_);
             const int fy = first_node<1>(y, fy_);
             const int fz = first_node<1>(z, fz_);
+            {
+                // fast path: the cell is one of the tile's own; then x, y, z are in
+                // the domain too (a NaN or out-of-range coordinate fails the test)
+                const unsigned dx = (unsigned)(fx - ox), dy = (unsigned)(fy - oy), dz = (unsigned)(fz - oz);
+                if ((C::KLO == 0) & (dx < (unsigned)C::KHI) & (dy < (unsigned)C::KHI) & (dz < (unsigned)C::KHI)) {
+                    const int k = ((int)dz * C::KR + (int)dy) * C::KR + (int)dx;
+                    const unsigned r = atomicAdd(&cnt[k], 1u);
+                    if (r < (unsigned)CAP) {
+                        float2 *dst = st + r * NK + k;
+                        dst[0] = make_float2(fx_, fy_);
+                        dst[CAP * NK] = make_float2(fz_, qvx);
+                        dst[2 * CAP * NK] = make_float2(qvy, qvz);
+                    } else {
+                        to_list((int)dx, (int)dy, (int)dz, fx_, fy_, fz_, qvx, qvy, qvz);
+                    }
+                    continue;
+                }
+            }
+            if (!in_domain<3>(g, x, y, z)) {
+                ++n_inv;
+                continue;
+            }
             const int lx = local_index<2, 8, HALO>(fx, ox, g.N[0]);
             const int ly = local_index<2, 8, HALO>(fy, oy, g.N[1]);
             const int lz = local_index<2, 8, HALO>(fz, oz, g.N[2]);
@@ -966,23 +1016,11 @@ __global__ void __launch_bounds__(512, 1)
                                   (lz >= -HALO) & (lz + 1 < 8 + HALO);
                 if (!fits) {
                     ++n_esc;
-                    deposit_global<3, 1>(g, J, x, y, z, qvx, qvy, qvz);
+                    escape_to_global(g, J, x, y, z, qvx, qvy, qvz);
                     continue;
                 }
             }
-            const unsigned hs = atomicAdd(&hcount[parity], 1u);
-            if (hs < (unsigned)HCAP) {
-                hbuf[0 * HCAP + hs] = fx_;
-                hbuf[1 * HCAP + hs] = fy_;
-                hbuf[2 * HCAP + hs] = fz_;
-                hbuf[3 * HCAP + hs] = qvx;
-                hbuf[4 * HCAP + hs] = qvy;
-                hbuf[5 * HCAP + hs] = qvz;
-                hbuf[6 * HCAP + hs] = __int_as_float(((lx + HALO) & 255) | (((ly + HALO) & 255) << 8) |
-                                                     (((lz + HALO) & 255) << 16));
-            } else {
-                stencil_to_global<HALO>(g, J, ox, oy, oz, lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
-            }
+            to_list(lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
         }
         // ---- the next round: position, and its particles into registers ----
         RoundPos nxt = cur;
@@ -1003,21 +1041,17 @@ __global__ void __launch_bounds__(512, 1)
                 const float2 a = st[r * NK + tid];
                 const float2 b = st[CAP * NK + r * NK + tid];
                 const float2 c = st[2 * CAP * NK + r * NK + tid];
-                const float wx[2] = {1.f - a.x, a.x}, wy[2] = {1.f - a.y, a.y}, wz[2] = {1.f - b.x, b.x};
+                // moments sum qv fx^i fy^j fz^k (i, j, k in {0, 1}) in acc[i + 2j + 4k]
+                const float fx = a.x, fy = a.y, fz = b.x;
+                const float fxy = fx * fy, fxz = fx * fz, fyz = fy * fz, fxyz = fxy * fz;
+                const float mono[8] = {1.f, fx, fy, fxy, fz, fxz, fyz, fxyz};
+                const float qv[3] = {b.y, c.x, c.y};
 #pragma unroll
-                for (int kz = 0; kz < 2; ++kz)
+                for (int comp = 0; comp < 3; ++comp) {
+                    acc[0][comp] += qv[comp];
 #pragma unroll
-                    for (int ky = 0; ky < 2; ++ky) {
-                        const float wyz = wy[ky] * wz[kz];
-#pragma unroll
-                        for (int kx = 0; kx < 2; ++kx) {
-                            const float W = wyz * wx[kx];
-                            float *ac = acc[(kz * 2 + ky) * 2 + kx];
-                            ac[0] = fmaf(b.y, W, ac[0]);
-                            ac[1] = fmaf(c.x, W, ac[1]);
-                            ac[2] = fmaf(c.y, W, ac[2]);
-                        }
-                    }
+                    for (int i = 1; i < 8; ++i) acc[i][comp] = fmaf(qv[comp], mono[i], acc[i][comp]);
+                }
             }
         }
         {
@@ -1038,6 +1072,15 @@ __global__ void __launch_bounds__(512, 1)
             float *corner = reinterpret_cast<float *>(st);  // [24][NK]
             __syncthreads();  // every cell's staged particles have been read
             if (tid < NK) {
+                // moments -> corner weights: along each axis the CIC weights are
+                // 1 - f and f, so the low corner is M0 - M1 and the high one M1
+#pragma unroll
+                for (int comp = 0; comp < 3; ++comp)
+#pragma unroll
+                    for (int bit = 1; bit < 8; bit <<= 1)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (!(i & bit)) acc[i][comp] -= acc[i | bit][comp];
 #pragma unroll
                 for (int a = 0; a < 8; ++a)
 #pragma unroll
