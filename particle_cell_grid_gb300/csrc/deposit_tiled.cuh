@@ -962,6 +962,9 @@ __global__ void __launch_bounds__(512, 1)
         ox = tx * 8;
         oy = ty * 8;
         oz = tz * 8;
+        // the tile's own cells that exist (a last tile may stick out of the grid)
+        const unsigned limx = (unsigned)min(C::KHI, g.N[0] - ox), limy = (unsigned)min(C::KHI, g.N[1] - oy),
+                       limz = (unsigned)min(C::KHI, g.N[2] - oz);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const long long p = cur.rb + (j >> 2) * (K::R / 2) + 4 * tid + (j & 3);
@@ -974,10 +977,12 @@ __global__ void __launch_bounds__(512, 1)
             const int fy = first_node<1>(y, fy_);
             const int fz = first_node<1>(z, fz_);
             {
-                // fast path: the cell is one of the tile's own; then x, y, z are in
-                // the domain too (a NaN or out-of-range coordinate fails the test)
+                // fast path: the cell is one of the tile's own cells inside the grid
+                // and the coordinates are not negative (the conversion truncates
+                // towards zero); then x, y, z are in the domain (a NaN fails too)
                 const unsigned dx = (unsigned)(fx - ox), dy = (unsigned)(fy - oy), dz = (unsigned)(fz - oz);
-                if ((C::KLO == 0) & (dx < (unsigned)C::KHI) & (dy < (unsigned)C::KHI) & (dz < (unsigned)C::KHI)) {
+                if ((C::KLO == 0) & (x >= 0.f) & (y >= 0.f) & (z >= 0.f) & (dx < limx) & (dy < limy) &
+                    (dz < limz)) {
                     const int k = ((int)dz * C::KR + (int)dy) * C::KR + (int)dx;
                     const unsigned r = atomicAdd(&cnt[k], 1u);
                     if (r < (unsigned)CAP) {
@@ -1037,6 +1042,7 @@ __global__ void __launch_bounds__(512, 1)
             const unsigned m0 = cnt[tid];
             const unsigned m = m0 < (unsigned)CAP ? m0 : (unsigned)CAP;
             cnt[tid] = 0;
+#pragma unroll 2
             for (unsigned r = 0; r < m; ++r) {
                 const float2 a = st[r * NK + tid];
                 const float2 b = st[CAP * NK + r * NK + tid];

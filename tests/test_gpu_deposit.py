@@ -116,6 +116,31 @@ def test_invalid_particles_skipped_and_tail_pass():
         assert st["n_invalid"] == ninv == 60
 
 
+@pytest.mark.parametrize("halo", [1, 2])
+def test_drift_out_of_domain_in_a_partial_last_tile(halo):
+    # grid edges not multiples of the tile: the last tile along each axis sticks
+    # out of the grid; particles sorted inside it whose deposit position drifted
+    # past N (or below 0 in the first tile) are invalid, not deposited
+    pcg = need_gpu()
+    grid = (20, 19, 21)
+    rng = np.random.default_rng(31)
+    n = 30000
+    kp = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    vel = [rng.normal(0, 0.05, n).astype(np.float32) for _ in range(3)]
+    q = rng.choice([-1.0, 1.0], n).astype(np.float32)
+    pos = [k.copy() for k in kp]
+    for mu, N in enumerate(grid):
+        hi = np.flatnonzero(kp[mu] > N - 1)[:50]
+        pos[mu][hi] = np.float32(N) + rng.uniform(0, 0.9, hi.size).astype(np.float32)  # drifted past N
+        lo = np.flatnonzero(kp[mu] < 1)[:50]
+        pos[mu][lo] = -rng.uniform(0.01, 0.9, lo.size).astype(np.float32)  # drifted below 0
+    J, st = _deposit(pcg, grid, 1, pos, vel, q, tile=8, halo=halo, key_pos=kp)
+    Jr, ninv = oracle.deposit_current(grid, 1, pos, vel, q)
+    assert ninv > 200
+    assert_deposit_close(J, Jr)
+    assert st["n_invalid"] == ninv
+
+
 def test_tail_pass_deposits_particles_that_were_invalid_at_sort_time():
     # keys from positions that were out of the domain at sort time, deposit
     # positions inside: those slots form the tail and go through the flat path
