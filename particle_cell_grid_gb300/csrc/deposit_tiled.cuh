@@ -484,254 +484,6 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
 }
 
 // ---------------------------------------------------------------------------
-// 3D CIC with 8^3 tiles: one thread per cell of the tile (512 threads).
-// Each thread keeps its cell's 8 corners x 3 components in registers for the
-// whole tile segment and adds them to the scratch tile once at the end (32
-// consecutive threads -> 32 consecutive cells: distinct banks).  A sub-batch of
-// two particles per thread is distributed to its cells through a transposed
-// staging array stage[field][rank][cell]: the placing atomic returns the rank,
-// and each cell's thread reads rank r of all 32 cells of its warp from 32
-// consecutive words.  A cell holds up to CAP particles per sub-batch; further
-// ones, and particles that drifted into the halo, go to a short list that
-// densely packed threads deposit with per-particle shared reductions.
-// ---------------------------------------------------------------------------
-template <int HALO>
-struct Cic3Cfg {
-    static constexpr int THREADS = 512;
-    static constexpr int PAIRS = THREADS;          // one pair of particles per thread
-    static constexpr int CAP = 6;                  // staged particles per cell and sub-batch
-    static constexpr int HCAP = 256;               // listed halo / overflow particles
-    using C = TileCfg<3, 1, 8, HALO>;
-    static constexpr int NK = C::NKEYS;            // cells whose stencil fits the window
-};
-
-template <int HALO, int MINB>
-__global__ void __launch_bounds__(512, MINB)
-    deposit_cic3d_kernel(Geom g, Particles P, long long n, const uint32_t *__restrict__ offs,
-                         const unsigned *__restrict__ chunk_tile, long long chunk,
-                         float *__restrict__ J, Counters ctr, bool vec) {
-    using K = Cic3Cfg<HALO>;
-    using C = typename K::C;
-    constexpr int NK = K::NK;
-    extern __shared__ __align__(16) unsigned char dsm[];
-    float *scratch = reinterpret_cast<float *>(dsm);                    // [3][CELLS]
-    float *stage = scratch + C::FLOATS;                                  // [6][CAP][NK]
-    float *hbuf = stage + 6 * K::CAP * NK;                               // [7][HCAP]
-    unsigned *cnt = reinterpret_cast<unsigned *>(hbuf + 7 * K::HCAP);   // [NK]
-    __shared__ unsigned hcount[2];
-
-    const int tid = threadIdx.x;
-    const long long c0 = (long long)blockIdx.x * chunk;
-    const long long c1 = min(n, c0 + chunk);
-    unsigned n_esc = 0, n_inv = 0;
-    unsigned t = chunk_tile[blockIdx.x];
-    if (t > g.n_tiles) t = g.n_tiles;
-    // this thread's cell (key) and its local first node
-    const int kx0 = tid % C::KR + C::KLO, ky0 = (tid / C::KR) % C::KR + C::KLO,
-              kz0 = tid / (C::KR * C::KR) + C::KLO;
-    for (;; ++t) {
-        long long s = (long long)offs[t];
-        if (s < c0) s = c0;
-        if (s >= c1) break;
-        long long e = (t < g.n_tiles) ? (long long)offs[t + 1] : c1;
-        if (e > c1) e = c1;
-        if (t == g.n_tiles) {
-            for (long long p = s + tid; p < e; p += K::THREADS) {
-                const float x = P.x[p], y = P.y[p], z = P.z[p];
-                if (!in_domain<3>(g, x, y, z)) {
-                    ++n_inv;
-                    continue;
-                }
-                const float q = P.q[p];
-                deposit_global<3, 1>(g, J, x, y, z, q * P.vx[p], q * P.vy[p], q * P.vz[p]);
-            }
-            break;
-        }
-        if (e <= s) continue;
-        const int tx = (int)(t % (unsigned)g.nt[0]);
-        const int ty = (int)((t / (unsigned)g.nt[0]) % (unsigned)g.nt[1]);
-        const int tz = (int)(t / ((unsigned)g.nt[0] * (unsigned)g.nt[1]));
-        const int ox = tx * 8, oy = ty * 8, oz = tz * 8;
-
-        for (int i = tid; i < C::FLOATS; i += K::THREADS) scratch[i] = 0.f;
-        if (tid < NK) cnt[tid] = 0;
-        if (tid < 2) hcount[tid] = 0;
-        float acc[2][2][2][3];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) acc[a >> 2][(a >> 1) & 1][a & 1][0] = acc[a >> 2][(a >> 1) & 1][a & 1][1] =
-            acc[a >> 2][(a >> 1) & 1][a & 1][2] = 0.f;
-        __syncthreads();
-
-        const long long q0 = s >> 1, q1 = (e + 1) >> 1;  // pairs of slots
-        int parity = 0;
-        for (long long qb = q0; qb < q1; qb += K::PAIRS, parity ^= 1) {
-            // ---- A: load a pair, classify, place grouped particles by rank ----
-            {
-                const long long qi = qb + tid;
-                const long long p = qi << 1;
-                float xs[2], ys[2], zs[2], vxs[2], vys[2], vzs[2], qs[2];
-                if (qi < q1 && vec && p + 1 < n) {
-                    const float2 a = *reinterpret_cast<const float2 *>(P.x + p);
-                    const float2 b = *reinterpret_cast<const float2 *>(P.y + p);
-                    const float2 c = *reinterpret_cast<const float2 *>(P.z + p);
-                    const float2 d = *reinterpret_cast<const float2 *>(P.vx + p);
-                    const float2 f = *reinterpret_cast<const float2 *>(P.vy + p);
-                    const float2 h = *reinterpret_cast<const float2 *>(P.vz + p);
-                    const float2 k = *reinterpret_cast<const float2 *>(P.q + p);
-                    xs[0] = a.x; xs[1] = a.y; ys[0] = b.x; ys[1] = b.y; zs[0] = c.x; zs[1] = c.y;
-                    vxs[0] = d.x; vxs[1] = d.y; vys[0] = f.x; vys[1] = f.y; vzs[0] = h.x; vzs[1] = h.y;
-                    qs[0] = k.x; qs[1] = k.y;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const long long pj = (qi < q1 && p + j >= s && p + j < e) ? p + j : s;
-                        xs[j] = P.x[pj]; ys[j] = P.y[pj]; zs[j] = P.z[pj];
-                        vxs[j] = P.vx[pj]; vys[j] = P.vy[pj]; vzs[j] = P.vz[pj]; qs[j] = P.q[pj];
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const long long pj = p + j;
-                    if (qi >= q1 || pj < s || pj >= e) continue;
-                    const float x = xs[j], y = ys[j], z = zs[j];
-                    if (!in_domain<3>(g, x, y, z)) {
-                        ++n_inv;
-                        continue;
-                    }
-                    const float qq = qs[j];
-                    const float qvx = qq * vxs[j], qvy = qq * vys[j], qvz = qq * vzs[j];
-                    float fx_, fy_, fz_;
-                    const int fx = first_node<1>(x, fx_);
-                    const int fy = first_node<1>(y, fy_);
-                    const int fz = first_node<1>(z, fz_);
-                    const int lx = local_index<2, 8, HALO>(fx, ox, g.N[0]);
-                    const int ly = local_index<2, 8, HALO>(fy, oy, g.N[1]);
-                    const int lz = local_index<2, 8, HALO>(fz, oz, g.N[2]);
-                    const bool home = (lx >= C::KLO) & (lx < C::KHI) & (ly >= C::KLO) & (ly < C::KHI) &
-                                      (lz >= C::KLO) & (lz < C::KHI);
-                    if (home) {
-                        const int k = ((lz - C::KLO) * C::KR + (ly - C::KLO)) * C::KR + (lx - C::KLO);
-                        const unsigned r = atomicAdd(&cnt[k], 1u);
-                        if (r < (unsigned)K::CAP) {
-                            float *dst = stage + r * NK + k;
-                            dst[0 * K::CAP * NK] = fx_;
-                            dst[1 * K::CAP * NK] = fy_;
-                            dst[2 * K::CAP * NK] = fz_;
-                            dst[3 * K::CAP * NK] = qvx;
-                            dst[4 * K::CAP * NK] = qvy;
-                            dst[5 * K::CAP * NK] = qvz;
-                            continue;
-                        }
-                        // more than CAP in this cell: listed below like a halo particle
-                    } else {
-                        const bool fits = (lx >= -HALO) & (lx + 1 < 8 + HALO) & (ly >= -HALO) &
-                                          (ly + 1 < 8 + HALO) & (lz >= -HALO) & (lz + 1 < 8 + HALO);
-                        if (!fits) {
-                            ++n_esc;
-                            deposit_global<3, 1>(g, J, x, y, z, qvx, qvy, qvz);
-                            continue;
-                        }
-                    }
-                    const unsigned hs = atomicAdd(&hcount[parity], 1u);
-                    if (hs < (unsigned)K::HCAP) {
-                        hbuf[0 * K::HCAP + hs] = fx_;
-                        hbuf[1 * K::HCAP + hs] = fy_;
-                        hbuf[2 * K::HCAP + hs] = fz_;
-                        hbuf[3 * K::HCAP + hs] = qvx;
-                        hbuf[4 * K::HCAP + hs] = qvy;
-                        hbuf[5 * K::HCAP + hs] = qvz;
-                        hbuf[6 * K::HCAP + hs] = __int_as_float(((lx + HALO) & 255) | (((ly + HALO) & 255) << 8) |
-                                                                (((lz + HALO) & 255) << 16));
-                    } else {
-                        scratch_particle<3, 1, 8, HALO>(scratch, lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
-                    }
-                }
-            }
-            __syncthreads();
-
-            // pull the next sub-batch into L2 while this one is reduced
-            if (tid == 32 && vec) {
-                const long long nb0 = (qb + K::PAIRS) << 1;
-                long long nb1 = nb0 + 2 * K::PAIRS;
-                if (nb1 > (e & ~3ll)) nb1 = e & ~3ll;
-                const long long a0 = nb0 & ~3ll;
-                if (nb1 > a0) {
-                    const unsigned bytes = (unsigned)((nb1 - a0) * 4);
-                    prefetch_l2_bulk(P.x + a0, bytes);
-                    prefetch_l2_bulk(P.y + a0, bytes);
-                    prefetch_l2_bulk(P.z + a0, bytes);
-                    prefetch_l2_bulk(P.vx + a0, bytes);
-                    prefetch_l2_bulk(P.vy + a0, bytes);
-                    prefetch_l2_bulk(P.vz + a0, bytes);
-                    prefetch_l2_bulk(P.q + a0, bytes);
-                }
-            }
-            // ---- D: every cell's thread adds its staged particles in registers ----
-            if (tid == 0) hcount[parity ^ 1] = 0;  // the list the next sub-batch fills
-            if (tid < NK) {
-                const unsigned m = cnt[tid];
-                const unsigned mm = m < (unsigned)K::CAP ? m : (unsigned)K::CAP;
-                for (unsigned r = 0; r < mm; ++r) {
-                    const float *src = stage + r * NK + tid;
-                    const float ax = src[0 * K::CAP * NK], ay = src[1 * K::CAP * NK],
-                                az = src[2 * K::CAP * NK];
-                    const float a = src[3 * K::CAP * NK], b = src[4 * K::CAP * NK],
-                                c = src[5 * K::CAP * NK];
-                    const float wx[2] = {1.f - ax, ax}, wy[2] = {1.f - ay, ay}, wz[2] = {1.f - az, az};
-#pragma unroll
-                    for (int kz = 0; kz < 2; ++kz)
-#pragma unroll
-                        for (int ky = 0; ky < 2; ++ky) {
-                            const float wyz = wy[ky] * wz[kz];
-#pragma unroll
-                            for (int kx = 0; kx < 2; ++kx) {
-                                const float W = wyz * wx[kx];
-                                acc[kz][ky][kx][0] = fmaf(a, W, acc[kz][ky][kx][0]);
-                                acc[kz][ky][kx][1] = fmaf(b, W, acc[kz][ky][kx][1]);
-                                acc[kz][ky][kx][2] = fmaf(c, W, acc[kz][ky][kx][2]);
-                            }
-                        }
-                }
-                cnt[tid] = 0;
-            }
-            {
-                const unsigned nh = min(hcount[parity], (unsigned)K::HCAP);
-                for (unsigned h = tid; h < nh; h += K::THREADS) {
-                    const int pk = __float_as_int(hbuf[6 * K::HCAP + h]);
-                    scratch_particle<3, 1, 8, HALO>(scratch, (pk & 255) - HALO, ((pk >> 8) & 255) - HALO,
-                                                    ((pk >> 16) & 255) - HALO, hbuf[h], hbuf[K::HCAP + h],
-                                                    hbuf[2 * K::HCAP + h], hbuf[3 * K::HCAP + h],
-                                                    hbuf[4 * K::HCAP + h], hbuf[5 * K::HCAP + h]);
-                }
-            }
-            __syncthreads();
-        }
-
-        // ---- each cell's corners into the scratch tile once ----
-        if (tid < NK) {
-            const int base = ((kz0 + HALO) * C::TE + (ky0 + HALO)) * C::TE + (kx0 + HALO);
-#pragma unroll
-            for (int kz = 0; kz < 2; ++kz)
-#pragma unroll
-                for (int ky = 0; ky < 2; ++ky) {
-                    float *row = scratch + base + (kz * C::TE + ky) * C::TE;
-#pragma unroll
-                    for (int kx = 0; kx < 2; ++kx) {
-                        red_shared_add_f32(row + kx, acc[kz][ky][kx][0]);
-                        red_shared_add_f32(row + C::CELLS + kx, acc[kz][ky][kx][1]);
-                        red_shared_add_f32(row + 2 * C::CELLS + kx, acc[kz][ky][kx][2]);
-                    }
-                }
-        }
-        __syncthreads();
-        flush_scratch<3, 8, HALO, K::THREADS>(g, scratch, J, ox, oy, oz);
-        __syncthreads();
-    }
-    warp_add_u64(ctr.n_escaped, n_esc);
-    warp_add_u64(ctr.n_invalid, n_inv);
-}
-
-// ---------------------------------------------------------------------------
 // 3D CIC with 8^3 tiles, persistent: one CTA of 512 threads per SM walks the
 // chunks b, b + grid, ... of the tile-sorted array in rounds of 4096
 // particles (8 per thread, loaded as float4 per field).  One thread per cell of
@@ -1153,32 +905,6 @@ pcg_status launch_cic3d_v5(const Geom &g, long long n, const Particles &P, const
     return launch_status();
 }
 
-template <int HALO>
-pcg_status launch_cic3d(const Geom &g, long long n, const Particles &P, const uint32_t *offs,
-                        float *J, const Counters &ctr, const unsigned *chunk_tile, long long chunk,
-                        int minb, cudaStream_t s) {
-    using K = Cic3Cfg<HALO>;
-    const long long nchunks = (n + chunk - 1) / chunk;
-    if (nchunks == 0) return PCG_OK;
-    const bool vec = aligned16(P.x) && aligned16(P.y) && aligned16(P.z) && aligned16(P.vx) &&
-                     aligned16(P.vy) && aligned16(P.vz) && aligned16(P.q);
-    const size_t smem = (size_t)K::C::FLOATS * 4 + (size_t)6 * K::CAP * K::NK * 4 +
-                        (size_t)7 * K::HCAP * 4 + (size_t)K::NK * 4;
-    if (minb == 1) {
-        PCG_CHECK_CUDA(cudaFuncSetAttribute(deposit_cic3d_kernel<HALO, 1>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        prof::Mark mk("deposit_tiled", s);
-        deposit_cic3d_kernel<HALO, 1><<<(unsigned)nchunks, K::THREADS, smem, s>>>(
-            g, P, n, offs, chunk_tile, chunk, J, ctr, vec);
-        return launch_status();
-    }
-    PCG_CHECK_CUDA(cudaFuncSetAttribute(deposit_cic3d_kernel<HALO, 2>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    prof::Mark mk("deposit_tiled", s);
-    deposit_cic3d_kernel<HALO, 2><<<(unsigned)nchunks, K::THREADS, smem, s>>>(g, P, n, offs, chunk_tile,
-                                                                              chunk, J, ctr, vec);
-    return launch_status();
-}
 
 template <int DIM, int ORDER, int TILE, int HALO, int THREADS>
 size_t tiled_smem() {
