@@ -6,7 +6,8 @@ Headline workload (one "step" = the whole current-deposit path on one batch):
   cell (268,435,456 particles), sort-time positions x_s, deposit positions
   x = x_s + v (0.1 % displaced by up to 3 cells), 8^3 tiles, 2-cell halo.
   step = tile counting sort (key, count, scan, permute) + tiled deposit
-  (scratch tile, escape valve, flush).  Inputs stay resident in HBM; they are
+  (per-cell register accumulation over each tile segment, escape valve, one
+  flush per node and tile).  Inputs stay resident in HBM; they are
   far larger than L2 (7.5 GB vs 129 MB), so no L2 flush is needed between steps.
 
 Also measured in the same run (the other rows of the hot path, each on its own
@@ -252,6 +253,15 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
     ms = dist.max(ms)
     res = {"n": n, "ms_per_step": ms / steps, "value": n * steps * dist.world / (ms * 1e-3) / 1e6,
            "escaped_per_step": st["n_escaped"], "invalid": st["n_invalid"], "profile": timed}
+    # load balance: particles per tile (the sentinel bin of invalid particles excluded)
+    tiles = np.diff(offs.cpu().numpy().astype(np.int64)[:nt + 1])[:nt]
+    res["tile_load"] = {"max": int(tiles.max()), "mean": round(float(tiles.mean()), 1),
+                        "max_over_mean": round(float(tiles.max() / max(tiles.mean(), 1e-30)), 2)}
+    # stencil node updates the deposit performs per second: (order + 1)^dim x 3 components per particle
+    dep = timed.get("deposit_tiled")
+    if dep:
+        upd = n * (d["order"] + 1) ** dim * 3
+        res["stencil_updates_per_s"] = round(upd / (dep[1] / dep[0] * 1e-3), 1)
     # algorithmic bytes per launch of the main kernels
     kbytes = 4 * dim * (1 if separate_keys else 0)
     node_bytes = 12 * int(np.prod(grid))
@@ -412,6 +422,7 @@ def run_gpu(args):
         "kernels": main["kernels"],
         "profile_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in main["profile"].items()},
         "escaped_per_step": main["escaped_per_step"],
+        "tile_load": main["tile_load"],
         "gpu_launches": main["gpu_launches"],
         "clocks": clocks,
     }
@@ -433,7 +444,8 @@ def run_gpu(args):
         wl["quad3d_bump_192"] = {"workload": "quad3d_bump 192^3, mean 32 ppc, peak 320", "particles": r4["n"],
                                  "value": round(r4["value"], 1), "unit": UNIT,
                                  "ms_per_step": round(r4["ms_per_step"], 4), "kernels": r4["kernels"],
-                                 "escaped_per_step": r4["escaped_per_step"]}
+                                 "escaped_per_step": r4["escaped_per_step"], "tile_load": r4["tile_load"],
+                                 "stencil_updates_per_s": r4.get("stencil_updates_per_s")}
         del d4
         wl["mass3d_64"] = mass_workload(pcg, ks, kw, dist, peaks, traffic)
         line["workloads"] = wl
