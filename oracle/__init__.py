@@ -56,6 +56,8 @@ def _load():
             lib.oracle_version.restype = ctypes.c_int
             lib.oracle_cic1d.restype = i64
             lib.oracle_cic1d.argtypes = [vp, vp, i64, vp, i32, i32, dbl, dbl, vp, vp]
+            lib.oracle_cic1d_grad.restype = i64
+            lib.oracle_cic1d_grad.argtypes = [vp, vp, i64, vp, i32, i32, dbl, dbl, vp, vp, vp]
             lib.oracle_axis_support.restype = ctypes.c_int
             lib.oracle_axis_support.argtypes = [i32, dbl, vp, vp]
             lib.oracle_deposit_current.restype = i64
@@ -95,6 +97,23 @@ def cic1d(x0, v, target, nbins=1024, nsteps=50, dt=0.01, halfwidth=0.005):
     nsel = lib.oracle_cic1d(_ptr(x0), _ptr(v), x0.size, _ptr(target), nbins, nsteps,
                             float(dt), float(halfwidth), _ptr(H), _ptr(loss))
     return H, float(loss[0]), int(nsel)
+
+
+def cic1d_grad(x0, v, target, nbins=1024, nsteps=50, dt=0.01, halfwidth=0.005):
+    """Gradient of the 1D loss with respect to x0 (the page's d L / d x0).
+
+    Returns (dx0 float64[n], H float64[nbins], loss, n_deposits); follows
+    "03. Compaction and scatter-add", "The problem" and "Code" (reverse pass
+    seeded with dL/dH = 2 (H - target))."""
+    lib = _load()
+    x0, v, target = _f32(x0), _f32(v), _f32(target)
+    assert x0.shape == v.shape and target.shape == (nbins,)
+    H = np.zeros(nbins, dtype=np.float64)
+    loss = np.zeros(1, dtype=np.float64)
+    dx0 = np.zeros(x0.size, dtype=np.float64)
+    nsel = lib.oracle_cic1d_grad(_ptr(x0), _ptr(v), x0.size, _ptr(target), nbins, nsteps, float(dt),
+                                 float(halfwidth), _ptr(H), _ptr(loss), _ptr(dx0))
+    return dx0, H, float(loss[0]), int(nsel)
 
 
 def axis_support(order, x):

@@ -87,6 +87,48 @@ int64_t oracle_cic1d(const float *x0, const float *v, int64_t n,
     return nsel;
 }
 
+/* Gradient of the 1D loss with respect to the initial positions, the
+ * quantity the page differentiates ("03. Compaction and scatter-add", "The
+ * problem": d L / d x0; "Code": the reverse pass is seeded with
+ * dL/dH = 2 (H - target)).  The window test, the wrap and floor(g) are
+ * piecewise constant; along x = wrap(x0 + v s) the derivative of every
+ * selected (particle, step) term follows from
+ *   d = minimg(x - c):  dd/dx0 = 1,
+ *   w = (1 - |d|/h)^2:  dw/dd  = -2 (1 - |d|/h) sign(d) / h   (sign(0) = 0),
+ *   f = x*nb - 1/2 - floor(.):  df/dx0 = nb,
+ * so the pair H[j] += w (1 - f), H[j+1] += w f contributes
+ *   G[j] (w' (1 - f) - w nb) + G[j+1] (w' f + w nb),  G = 2 (H - target).
+ * H is the fp64 forward result of oracle_cic1d; dx0 is written for every
+ * particle (zero for particles never selected).  Returns the selected count. */
+int64_t oracle_cic1d_grad(const float *x0, const float *v, int64_t n,
+                          const float *target, int32_t nbins, int32_t nsteps,
+                          double dt, double hw, double *H, double *loss, double *dx0) {
+    int64_t nsel = oracle_cic1d(x0, v, n, target, nbins, nsteps, dt, hw, H, loss);
+    for (int64_t p = 0; p < n; ++p) dx0[p] = 0.0;
+    for (int32_t t = 1; t <= nsteps; ++t) {
+        double c = (double)t / (double)nsteps;
+        double s = (double)t * dt;
+        for (int64_t p = 0; p < n; ++p) {
+            double xu = (double)x0[p] + (double)v[p] * s;
+            double x = xu - floor(xu);
+            double d = minimg(x - c);
+            if (!(fabs(d) < hw)) continue;
+            double u = 1.0 - fabs(d) / hw;
+            double w = u * u;
+            double sgn = d > 0.0 ? 1.0 : (d < 0.0 ? -1.0 : 0.0);
+            double dw = -2.0 * u * sgn / hw;
+            double g = x * (double)nbins - 0.5;
+            double jf = floor(g);
+            double f = g - jf;
+            int64_t j = (int64_t)jf;
+            double G0 = 2.0 * (H[mod_floor(j, nbins)] - (double)target[mod_floor(j, nbins)]);
+            double G1 = 2.0 * (H[mod_floor(j + 1, nbins)] - (double)target[mod_floor(j + 1, nbins)]);
+            dx0[p] += G0 * (dw * (1.0 - f) - w * (double)nbins) + G1 * (dw * f + w * (double)nbins);
+        }
+    }
+    return nsel;
+}
+
 /* ------------------------------------------------------------------------ */
 /* 1D B-spline weights (Pennati & Markidis, Sec. 2.3, Eq. (12))              */
 /* ------------------------------------------------------------------------ */

@@ -264,6 +264,60 @@ def test_cic1d_selection_count_and_mass():
     assert 0.35 <= ever.mean() <= 0.65
 
 
+@pytest.mark.parametrize("seed,nb,T,hw", [(5, 64, 20, 0.05), (6, 256, 50, 0.01), (7, 32, 8, 0.2)])
+def test_cic1d_gradient_matches_central_differences(seed, nb, T, hw):
+    # the gradient against central differences of the (separately pinned) loss;
+    # a step of 2^-20 is exact in fp32 for x0 in [0.5, 1)
+    rng = np.random.default_rng(seed)
+    n, dt = 48, 0.01
+    x0 = (0.5 + 0.5 * rng.random(n)).astype(np.float32)
+    v = rng.normal(0, 0.1, n).astype(np.float32)
+    target = rng.random(nb).astype(np.float32)
+    g, H, loss, nsel = oracle.cic1d_grad(x0, v, target, nb, T, dt, hw)
+    H1, loss1, nsel1 = oracle.cic1d(x0, v, target, nb, T, dt, hw)
+    assert nsel == nsel1 and loss == loss1 and np.array_equal(H, H1)
+    eps = np.float32(2.0 ** -20)
+    fd = np.zeros(n)
+    for i in range(n):
+        xp, xm = x0.copy(), x0.copy()
+        xp[i] += eps
+        xm[i] -= eps
+        fd[i] = (oracle.cic1d(xp, v, target, nb, T, dt, hw)[1] -
+                 oracle.cic1d(xm, v, target, nb, T, dt, hw)[1]) / (float(xp[i]) - float(xm[i]))
+    assert nsel > 0
+    # a particle within one step of a bin boundary sits on a kink of the loss
+    # (the CIC weight derivatives switch bins there) and the central difference
+    # averages the two sides; a wrong term would spoil nearly every particle
+    ok = np.abs(fd - g) <= 1e-6 * max(np.abs(g).max(), 1.0)
+    assert ok.mean() >= 0.95
+
+
+def test_cic1d_gradient_zero_for_unselected_and_linear_in_residual():
+    d = synth.cic1d()
+    args = (d["nbins"], d["nsteps"], d["dt"], d["halfwidth"])
+    g, H, loss, nsel = oracle.cic1d_grad(d["x0"], d["v"], d["target"], *args)
+    # particles never inside the window have an exactly zero gradient
+    x0 = d["x0"].astype(np.float64)
+    v = d["v"].astype(np.float64)
+    ever = np.zeros(x0.size, bool)
+    for t in range(1, d["nsteps"] + 1):
+        r = np.mod(np.mod(x0 + v * (t * d["dt"]), 1.0) - t / d["nsteps"], 1.0)
+        ever |= np.minimum(r, 1.0 - r) < d["halfwidth"]
+    assert (g[~ever] == 0).all() and (g[ever] != 0).sum() > 0.9 * ever.sum()
+    # dL/dx0 = sum_b 2 (H_b - target_b) dH_b/dx0 is affine in the target: the
+    # gradients at targets t_a and t_b average to the gradient at (t_a + t_b)/2
+    # (dyadic targets, so that the midpoint is exact in fp32)
+    rng = np.random.default_rng(1)
+    ta = (rng.integers(0, 1024, d["nbins"]) / 1024.0).astype(np.float32)
+    tb = (rng.integers(0, 1024, d["nbins"]) / 1024.0).astype(np.float32)
+    tm = ((ta.astype(np.float64) + tb) / 2).astype(np.float32)
+    assert np.array_equal(tm.astype(np.float64), (ta.astype(np.float64) + tb) / 2)
+    ga = oracle.cic1d_grad(d["x0"], d["v"], ta, *args)[0]
+    gb = oracle.cic1d_grad(d["x0"], d["v"], tb, *args)[0]
+    gm = oracle.cic1d_grad(d["x0"], d["v"], tm, *args)[0]
+    assert np.abs((ga + gb) / 2 - gm).max() <= 1e-9 * np.abs(ga).max()
+
+
 # ---------------------------------------------------------------------------
 # mass matrix: dense W S W^T on tiny grids, alpha closed forms and invariants
 # ---------------------------------------------------------------------------
