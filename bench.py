@@ -369,19 +369,29 @@ def mass_workload(pcg, steps, warmup, dist, peaks, traffic, edge=64):
 
 
 def cic1d_workload(pcg, steps, warmup, dist):
+    """The 1D windowed CIC histogram + loss, and its gradient dL/dx0, at the
+    pages' N = 2000 and at N = 10^7 (the size their gradient timings use)."""
     import torch
     import synth
-    d = synth.cic1d()
     dev = lambda a: torch.from_numpy(a).cuda()
-    x0, v, tg = dev(d["x0"]), dev(d["v"]), dev(d["target"])
-    H = torch.empty(d["nbins"], dtype=torch.float32, device="cuda")
-    L = torch.empty(1, dtype=torch.float64, device="cuda")
-    step = lambda: pcg.deposit_cic1d(x0, v, tg, d["nsteps"], d["dt"], d["halfwidth"], H=H, loss=L)
-    ms = time_steps(step, steps, warmup, dist, torch.cuda.current_stream())
-    us = ms * 1e3 / steps
-    return {"workload": "cic1d N=2000, 1024 bins, T=50", "us_per_call": round(us, 2),
-            "M_particle_steps_per_s": round(2000 * 50 / (us * 1e-6) / 1e6, 1),
-            "note": "latency-bound (16 KB in, 4 KB out): one cluster launch per call, no roofline fraction"}
+    out = {"workload": "cic1d 1024 bins, T=50, h=0.005"}
+    for n, k in ((2000, steps), (10_000_000, max(5, steps // 20))):
+        d = synth.cic1d(n=n)
+        x0, v, tg = dev(d["x0"]), dev(d["v"]), dev(d["target"])
+        H = torch.empty(d["nbins"], dtype=torch.float32, device="cuda")
+        L = torch.empty(1, dtype=torch.float64, device="cuda")
+        g = torch.empty(n, dtype=torch.float64, device="cuda")
+        args = (d["nsteps"], d["dt"], d["halfwidth"])
+        fwd = lambda: pcg.deposit_cic1d(x0, v, tg, *args, H=H, loss=L)
+        grad = lambda: pcg.deposit_cic1d_grad(x0, v, tg, *args, H=H, loss=L, dx0=g)
+        for name, step in (("forward", fwd), ("forward+grad", grad)):
+            us = time_steps(step, k, warmup, dist, torch.cuda.current_stream()) * 1e3 / k
+            out[f"N={n} {name}"] = {"us_per_call": round(us, 2),
+                                    "M_particle_steps_per_s": round(n * 50 / (us * 1e-6) / 1e6, 1)}
+        del x0, v, tg, g
+    out["note"] = ("N=2000: latency-bound, one cluster launch (+1 for the gradient); N=10^7: 80 MB of "
+                   "input, resident in L2 between calls, bound by the fp32 screen of 5e8 pairs")
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -433,7 +443,7 @@ def run_gpu(args):
     if dist.world == 1 and not args.main_only:
         wl = {}
         ks, kw = max(3, args.steps // 10), max(3, args.warmup)
-        wl["cic1d"] = cic1d_workload(pcg, 200, 10, dist)
+        wl["cic1d"] = cic1d_workload(pcg, 200, 5, dist)
         d2 = synth.cic2d()
         r2 = current_workload(pcg, d2, max(20, args.steps // 2), kw, dist, peaks, traffic)
         wl["cic2d_512"] = {"workload": "cic2d 512^2 x 8 ppc", "value": round(r2["value"], 1), "unit": UNIT,

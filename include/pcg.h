@@ -97,11 +97,36 @@ PCG_API pcg_status pcg_stats_check(const pcg_stats *host_stats);
  *   H        device float[nbins], output (overwritten).
  *   loss     device double[1], output (overwritten).
  *   n >= 0; 1 <= nbins <= 16384; nsteps >= 1; 0 < halfwidth; dt finite.
- * One launch of one 8-CTA thread-block cluster; no workspace.
+ * Up to 16384 particles: one launch of one 8-CTA thread-block cluster.  Above:
+ * a memset of H, one full-grid launch and a one-CTA loss launch.  No
+ * workspace.  The order of the fp32 additions into H is unspecified.
  */
 PCG_API pcg_status pcg_deposit_cic1d(const float *x0, const float *v, int64_t n, const float *target,
                              int32_t nbins, int32_t nsteps, double dt, double halfwidth,
                              float *H, double *loss, void *stream);
+
+/* -------------------------------------------------------------------------
+ * Gradient of the 1D windowed CIC loss with respect to the initial positions.
+ * Defined by "03. Compaction and scatter-add" (WEANJ examples), section "The
+ * problem" (dL/dx0 of the loss above) and section "Code" (the reverse pass is
+ * seeded with dL/dH = 2 (H - target)).  The wrap, the window test and floor(g)
+ * are piecewise constant and contribute no derivative, so every selected
+ * (particle, step) pair adds
+ *   G[b0] (w' (1 - f) - w nbins) + G[b1] (w' f + w nbins),
+ *   G = 2 (H - target),  w' = -2 (1 - |d|/h) sign(d) / h  (sign(0) = 0),
+ * to dx0 of its particle, b0/b1 and f the CIC bins and fraction above.
+ *
+ * Runs the forward pass of pcg_deposit_cic1d (same arguments, same H and
+ * loss), then the gradient, which reads H from the forward.
+ *   dx0      device double[n], output (overwritten; zero for particles never
+ *            selected).  May be NULL when n == 0.
+ * The selection is the forward's fp64 test, so both passes select the same
+ * pairs; G and the sum are in fp64 (pairs of one particle are added in an
+ * unspecified order).  One launch more than the forward.
+ */
+PCG_API pcg_status pcg_deposit_cic1d_grad(const float *x0, const float *v, int64_t n, const float *target,
+                                  int32_t nbins, int32_t nsteps, double dt, double halfwidth,
+                                  float *H, double *loss, double *dx0, void *stream);
 
 /* -------------------------------------------------------------------------
  * Tile counting sort.

@@ -7,7 +7,7 @@ provides device memory and streams.  Outputs not supplied by the caller are
 allocated with torch; workspaces likewise.
 
 Entry points (same names as the C ABI without the ``pcg_`` prefix):
-  deposit_cic1d, tile_sort, deposit_current, assemble_mass_matrix,
+  deposit_cic1d, deposit_cic1d_grad, tile_sort, deposit_current, assemble_mass_matrix,
   plus the *_workspace_size queries and stats helpers.
 """
 from __future__ import annotations
@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import PcgError, check
 
 __all__ = [
-    "PcgError", "version", "deposit_cic1d", "tile_sort", "tile_sort_workspace_size",
+    "PcgError", "version", "deposit_cic1d", "deposit_cic1d_grad", "tile_sort", "tile_sort_workspace_size",
     "deposit_current", "deposit_current_workspace_size", "assemble_mass_matrix",
     "assemble_mass_matrix_workspace_size", "new_stats", "read_stats", "n_tiles",
     "profile_enable", "profile_collect",
@@ -111,6 +111,23 @@ def deposit_cic1d(x0, v, target, nsteps=50, dt=0.01, halfwidth=0.005, H=None, lo
                                        float(dt), float(halfwidth), _ptr(H), _ptr(loss), _stream(stream))
     check(st, "pcg_deposit_cic1d")
     return H, loss
+
+
+def deposit_cic1d_grad(x0, v, target, nsteps=50, dt=0.01, halfwidth=0.005, H=None, loss=None, dx0=None,
+                       stream=None):
+    """Forward (H, loss) and dL/dx0 (float64[n]) of the 1D windowed CIC loss."""
+    _dev(x0, torch.float32, "x0")
+    _dev(v, torch.float32, "v")
+    _dev(target, torch.float32, "target")
+    nb = target.numel()
+    H = torch.empty(nb, dtype=torch.float32, device=target.device) if H is None else _dev(H, torch.float32, "H")
+    loss = torch.empty(1, dtype=torch.float64, device=target.device) if loss is None else _dev(loss, torch.float64, "loss")
+    dx0 = torch.empty(x0.numel(), dtype=torch.float64, device=target.device) if dx0 is None else _dev(dx0, torch.float64, "dx0")
+    st = _lib.load().pcg_deposit_cic1d_grad(_ptr(x0), _ptr(v), x0.numel(), _ptr(target), nb, int(nsteps),
+                                            float(dt), float(halfwidth), _ptr(H), _ptr(loss), _ptr(dx0),
+                                            _stream(stream))
+    check(st, "pcg_deposit_cic1d_grad")
+    return H, loss, dx0
 
 
 # ---------------------------------------------------------------------------

@@ -28,6 +28,7 @@ SIGNATURES = {
     "pcg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pcg_stats_check": (ctypes.c_int, [_vp]),
     "pcg_deposit_cic1d": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i32, _i32, _dbl, _dbl, _vp, _vp, _vp]),
+    "pcg_deposit_cic1d_grad": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i32, _i32, _dbl, _dbl, _vp, _vp, _vp, _vp]),
     "pcg_tile_sort_workspace_size": (ctypes.c_int, [_i32, _vp, _i32, _i64, _i32, _P(_sz)]),
     "pcg_tile_sort": (ctypes.c_int, [_i32, _vp, _i32, _i64, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "pcg_deposit_current_workspace_size": (ctypes.c_int, [_i32, _vp, _i32, _i64, _P(_sz)]),

@@ -1,25 +1,40 @@
-// cic1d.cu -- 1D windowed cloud-in-cell histogram and loss in one launch.
+// cic1d.cu -- 1D windowed cloud-in-cell histogram, loss and gradient.
 //
 // Method: "03. Compaction and scatter-add" (WEANJ examples), sections "The
 // problem" and "Code".  For every step t = 1..T the particles inside a window of
 // half-width h around c = t/T add a tapered weight w = (1 - |d|/h)^2 to the two
-// CIC bins of g = x*nb - 1/2; the loss is ||H - target||^2.
+// CIC bins of g = x*nb - 1/2; the loss is ||H - target||^2, and the gradient
+// dL/dx0 is seeded with dL/dH = 2 (H - target).
 //
 // GB300 design.  The pages launch one kernel per step (T launches) with global
-// atomics.  Here all T steps run in a single launch of one 8-CTA thread-block
-// cluster: each CTA keeps a private histogram in shared memory, the CTAs meet
-// at a hardware cluster barrier, and CTA 0 sums the eight histograms through
-// distributed shared memory in a fixed order, writes H and reduces the loss in
-// fp64.  No workspace, no global atomics, no counter to reset.
+// atomics and note that a stream-compaction pass before the deposit is what a
+// CUDA programmer would add ("Where JAX wins / what we did not do").  Here all
+// T steps run in one launch, and the compaction is done per warp, in shared
+// memory, on the fly:
+//   * every lane owns one particle of a 32-particle chunk and walks t = 1..T
+//     with a cheap fp32 window test (the screen);
+//   * the (particle, step) pairs that pass (~1% for h = 0.005) are appended to
+//     a 64-entry queue private to the warp (ballot + popc, no atomics, no
+//     block barrier);
+//   * whenever the queue holds 32 candidates the warp takes them together, one
+//     per lane, through the exact fp64 test and the deposit (or the gradient
+//     gather).  So the slow fp64 path always runs with all 32 lanes busy,
+//     instead of a few lanes of a diverged warp.
+// Small N: one 8-CTA thread-block cluster; each CTA keeps a private histogram in
+// shared memory, the CTAs meet at a cluster barrier and CTA 0 sums the eight
+// histograms through distributed shared memory in a fixed order, writes H and
+// reduces the loss in fp64 (one launch, no workspace).  Large N: a full grid of
+// CTAs, each adding its shared histogram to H with global reductions, then a
+// one-CTA loss kernel.  The gradient is a second kernel of the same shape that
+// gathers 2 (H - target) at the same two bins.
 //
 // Precision.  In fp32, x = x0 + v*t*dt carries ~6e-8 absolute error, i.e.
 // ~6e-5 of a bin after the scaling by nb = 1024, which would move CIC weights
 // by more than the 1e-5 tolerance; so the window test, g and floor(g) are done
 // in fp64 with individually rounded operations (the __d*_rn intrinsics are never
-// contracted into FMAs), exactly as the fp64 oracle does them.  fp64 is slow on
-// this part, so every (particle, step) pair first goes through an fp32 test
-// with a margin that provably covers the fp32 rounding; only the ~1% that pass
-// repeat the test in fp64.
+// contracted into FMAs), exactly as the fp64 oracle does them.  The fp32 screen
+// uses a margin that provably covers its own rounding, so it never drops a pair
+// the fp64 test would select.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -29,64 +44,148 @@ namespace cg = cooperative_groups;
 namespace pcg {
 namespace {
 
-constexpr int kCtas = 8;
-constexpr int kThreads = 256;
+constexpr int kCtas = 8;      // CTAs of the small-N cluster
+constexpr int kThreads = 256;  // threads of every CTA here
+constexpr int kWarps = kThreads / 32;
+constexpr int kQueue = 64;     // candidates a warp can hold (31 left over + 32 new, rounded up)
+// up to this many particles the histogram is built by the single 8-CTA
+// cluster; above it by a full grid with global reductions
+constexpr long long kClusterMaxN = 1ll << 14;
 
+// Per-launch constants of the method.
+struct Cic1dArgs {
+    const float *x0, *v;
+    long long n;
+    const float *target;
+    int nbins, nsteps;
+    double dt, hw;
+    float dt32, hw32, inv_t32;  // dt, h and 1/T rounded to fp32 for the screen
+};
+
+// fp32 screen of one (particle, step) pair.  |d32 - d64| stays below
+// ~6 ulp(1 + |x0| + |v s|) (the rounding of t*dt, v*s, x0 + v s, c and the
+// subtractions); the margin 2e-6 * (4 + |x0| + |v s|) is far above that, so
+// every pair the fp64 test selects passes.  When h + margin reaches 0.45 the
+// screen passes everything (both tests then reject |d| ~ 1/2 alike, where the
+// minimum image jumps).
+__device__ __forceinline__ bool cic1d_screen(const Cic1dArgs &a, float xf, float vf, int t) {
+    const float tf = (float)t;
+    const float vs32 = vf * (tf * a.dt32);
+    float d32 = (xf + vs32) - tf * a.inv_t32;
+    d32 = d32 - rintf(d32);
+    const float lim = a.hw32 + 2e-6f * (4.f + fabsf(xf) + fabsf(vs32));
+    return fabsf(d32) < lim || !(lim < 0.45f);
+}
+
+// One selected (particle, step) pair in fp64.
+struct Pair {
+    double d, u, w, f;  // minimum-image distance, 1 - |d|/h, taper, CIC fraction
+    int b0, b1;         // the two bins
+};
+
+// Exact fp64 window test and CIC weights, the same operation sequence as the
+// oracle: s = t dt, x = wrap(x0 + v s), d = minimg(x - t/T), |d| < h,
+// g = x nb - 1/2, f = g - floor(g).
+__device__ __forceinline__ bool cic1d_select(const Cic1dArgs &a, float xf, float vf, int t, Pair &o) {
+    const double s = __dmul_rn((double)t, a.dt);
+    const double xu = __dadd_rn((double)xf, __dmul_rn((double)vf, s));
+    const double x = __dsub_rn(xu, floor(xu));
+    const double c = __ddiv_rn((double)t, (double)a.nsteps);
+    const double d0 = __dsub_rn(x, c);
+    const double d = __dsub_rn(d0, rint(d0));
+    const double ad = fabs(d);
+    if (!(ad < a.hw)) return false;
+    o.d = d;
+    o.u = __dsub_rn(1.0, __ddiv_rn(ad, a.hw));
+    o.w = __dmul_rn(o.u, o.u);
+    const double g = __dsub_rn(__dmul_rn(x, (double)a.nbins), 0.5);
+    const double jf = floor(g);
+    o.f = __dsub_rn(g, jf);
+    int b0 = (int)jf % a.nbins;
+    if (b0 < 0) b0 += a.nbins;
+    o.b0 = b0;
+    o.b1 = b0 + 1 == a.nbins ? 0 : b0 + 1;
+    return true;
+}
+
+// Candidate queue of one warp, in shared memory.
+struct WarpQueue {
+    float2 xv[kQueue];      // x0 and v of the particle
+    int t[kQueue];          // step
+    long long p[kQueue];    // particle index (read by the gradient only)
+};
+
+// The warp walks the 32-particle chunks warp_id, warp_id + nwarps, ... (lane =
+// particle) over t = 1..T.  Pairs that pass the screen go to the warp's queue;
+// every time it holds 32 they are handed to take(x0, v, t, p) together, one
+// per lane; the last partial batch goes at the end.  on_load(p) runs once per
+// particle when its chunk is loaded.  The count of queued pairs is the same in
+// every lane (it only changes by popc of a ballot), so every branch on it is
+// warp-uniform and no block barrier is needed.
+template <bool kNeedP, class OnLoad, class Take>
+__device__ __forceinline__ void cic1d_walk(const Cic1dArgs &a, long long warp_id, long long nwarps,
+                                           WarpQueue &q, OnLoad on_load, Take take) {
+    const int lane = threadIdx.x & 31;
+    const unsigned below = (1u << lane) - 1u;
+    int count = 0;
+    for (long long base = warp_id * 32; base < a.n; base += nwarps * 32) {
+        const long long p = base + lane;
+        const bool live = p < a.n;
+        float xf = 0.f, vf = 0.f;
+        if (live) {
+            xf = a.x0[p];
+            vf = a.v[p];
+            on_load(p);
+        }
+        for (int t = 1; t <= a.nsteps; ++t) {
+            const bool pass = live && cic1d_screen(a, xf, vf, t);
+            const unsigned m = __ballot_sync(0xffffffffu, pass);
+            if (m == 0u) continue;
+            if (pass) {
+                const int slot = count + __popc(m & below);
+                q.xv[slot] = make_float2(xf, vf);
+                q.t[slot] = t;
+                if (kNeedP) q.p[slot] = p;
+            }
+            count += __popc(m);
+            if (count >= 32) {  // take the newest 32
+                count -= 32;
+                __syncwarp();
+                const int e = count + lane;
+                take(q.xv[e].x, q.xv[e].y, q.t[e], kNeedP ? q.p[e] : 0ll);
+                __syncwarp();
+            }
+        }
+    }
+    __syncwarp();
+    if (lane < count) take(q.xv[lane].x, q.xv[lane].y, q.t[lane], kNeedP ? q.p[lane] : 0ll);
+}
+
+// Deposit of one selected pair into the CTA's shared histogram.
+__device__ __forceinline__ void cic1d_deposit_pair(const Cic1dArgs &a, float *hist, float xf, float vf, int t) {
+    Pair pr;
+    if (!cic1d_select(a, xf, vf, t, pr)) return;
+    red_shared_add_f32(&hist[pr.b0], (float)__dmul_rn(pr.w, __dsub_rn(1.0, pr.f)));
+    red_shared_add_f32(&hist[pr.b1], (float)__dmul_rn(pr.w, pr.f));
+}
+
+// Small N: the whole histogram and the loss in one 8-CTA cluster.
 __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
-    cic1d_kernel(const float *__restrict__ x0, const float *__restrict__ v, long long n,
-                 const float *__restrict__ target, int nbins, int nsteps, double dt, double hw,
-                 float *__restrict__ H, double *__restrict__ loss) {
+    cic1d_cluster_kernel(Cic1dArgs a, float *__restrict__ H, double *__restrict__ loss) {
     extern __shared__ float hist[];  // [nbins]
-    __shared__ double red[kThreads / 32];
+    __shared__ WarpQueue queues[kWarps];
+    __shared__ double red[kWarps];
     cg::cluster_group cluster = cg::this_cluster();
     const unsigned rank = cluster.block_rank();
+    const int nbins = a.nbins;
 
     for (int b = threadIdx.x; b < nbins; b += kThreads) hist[b] = 0.f;
     __syncthreads();
 
-    const float dt32 = (float)dt;
-    const float hw32 = (float)hw;
-    const double inv_nb = (double)nbins;
-    const long long stride = (long long)kCtas * kThreads;
-    for (long long p = (long long)rank * kThreads + threadIdx.x; p < n; p += stride) {
-        const float xf = x0[p], vf = v[p];
-        const double xd = (double)xf, vd = (double)vf;
-        for (int t = 1; t <= nsteps; ++t) {
-            // fp32 screen.  |d32 - d64| <= ~6 ulp(1 + |x0| + |v s|); the margin is
-            // 2e-6 * (4 + |x0| + |v s|), far above that.  When h + margin reaches
-            // 0.45 the screen passes everything (both tests then reject |d| ~ 1/2
-            // alike, where minimg jumps).
-            const float s32 = (float)t * dt32;
-            const float vs32 = vf * s32;
-            const float c32 = (float)t / (float)nsteps;
-            float d32 = (xf + vs32) - c32;
-            d32 = d32 - rintf(d32);
-            const float margin = 2e-6f * (4.f + fabsf(xf) + fabsf(vs32));
-            const float lim = hw32 + margin;
-            if (!(fabsf(d32) < lim) && lim < 0.45f) continue;
-
-            // fp64 test, same operation sequence as the oracle
-            const double s = __dmul_rn((double)t, dt);
-            const double xu = __dadd_rn(xd, __dmul_rn(vd, s));
-            const double x = __dsub_rn(xu, floor(xu));
-            const double c = __ddiv_rn((double)t, (double)nsteps);
-            const double d0 = __dsub_rn(x, c);
-            const double d = __dsub_rn(d0, rint(d0));
-            const double ad = fabs(d);
-            if (!(ad < hw)) continue;
-            const double u = __dsub_rn(1.0, __ddiv_rn(ad, hw));
-            const double w = __dmul_rn(u, u);
-            const double g = __dsub_rn(__dmul_rn(x, inv_nb), 0.5);
-            const double jf = floor(g);
-            const double f = __dsub_rn(g, jf);
-            int j = (int)jf;
-            int b0 = j % nbins;
-            if (b0 < 0) b0 += nbins;
-            int b1 = b0 + 1 == nbins ? 0 : b0 + 1;
-            red_shared_add_f32(&hist[b0], (float)__dmul_rn(w, __dsub_rn(1.0, f)));
-            red_shared_add_f32(&hist[b1], (float)__dmul_rn(w, f));
-        }
-    }
+    const int warp = threadIdx.x >> 5;
+    cic1d_walk<false>(
+        a, (long long)rank * kWarps + warp, (long long)kCtas * kWarps, queues[warp], [](long long) {},
+        [&](float xf, float vf, int t, long long) { cic1d_deposit_pair(a, hist, xf, vf, t); });
 
     // all eight histograms complete and visible cluster-wide
     cluster.sync();
@@ -100,21 +199,150 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kThreads)
 #pragma unroll
             for (int r = 0; r < kCtas; ++r) sum += remote[r][b];
             H[b] = sum;
-            const double e = (double)sum - (double)target[b];
+            const double e = (double)sum - (double)a.target[b];
             acc = fma(e, e, acc);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+        if ((threadIdx.x & 31) == 0) red[warp] = acc;
         __syncthreads();
         if (threadIdx.x == 0) {
             double L = 0.0;
-            for (int w = 0; w < kThreads / 32; ++w) L += red[w];
+            for (int w = 0; w < kWarps; ++w) L += red[w];
             *loss = L;
         }
     }
     // keep every CTA's shared memory alive until CTA 0 has read it
     cluster.sync();
+}
+
+// Large N: every CTA builds a partial histogram and adds its non-zero bins to
+// H (zeroed before the launch) with global reductions.
+__global__ void __launch_bounds__(kThreads) cic1d_hist_kernel(Cic1dArgs a, float *__restrict__ H) {
+    extern __shared__ float hist[];  // [nbins]
+    __shared__ WarpQueue queues[kWarps];
+    const int nbins = a.nbins;
+    for (int b = threadIdx.x; b < nbins; b += kThreads) hist[b] = 0.f;
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    cic1d_walk<false>(
+        a, (long long)blockIdx.x * kWarps + warp, (long long)gridDim.x * kWarps, queues[warp],
+        [](long long) {}, [&](float xf, float vf, int t, long long) { cic1d_deposit_pair(a, hist, xf, vf, t); });
+    __syncthreads();
+    for (int b = threadIdx.x; b < nbins; b += kThreads) {
+        const float h = hist[b];
+        if (h != 0.f) red_add_f32(&H[b], h);
+    }
+}
+
+// loss = sum_b (H_b - target_b)^2 in fp64, one CTA.
+__global__ void __launch_bounds__(kThreads)
+    cic1d_loss_kernel(const float *__restrict__ H, const float *__restrict__ target, int nbins,
+                      double *__restrict__ loss) {
+    __shared__ double red[kWarps];
+    double acc = 0.0;
+    for (int b = threadIdx.x; b < nbins; b += kThreads) {
+        const double e = (double)H[b] - (double)target[b];
+        acc = fma(e, e, acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double L = 0.0;
+        for (int w = 0; w < kWarps; ++w) L += red[w];
+        *loss = L;
+    }
+}
+
+// Gradient: dx0[p] = sum over the selected steps of
+//   G[b0] (w' (1 - f) - w nb) + G[b1] (w' f + w nb),  G = 2 (H - target),
+// with w' = dw/dd = -2 u sign(d) / h and df/dx0 = nb (the wrap, the window
+// test and floor(g) are piecewise constant).  Every particle's entry is
+// zeroed when its chunk is loaded; pairs of the same particle can sit in one
+// batch, so they are added with fp64 atomics.
+__global__ void __launch_bounds__(kThreads)
+    cic1d_grad_kernel(Cic1dArgs a, const float *__restrict__ H, double *__restrict__ dx0) {
+    __shared__ WarpQueue queues[kWarps];
+    const int warp = threadIdx.x >> 5;
+    const double nb = (double)a.nbins;
+    cic1d_walk<true>(
+        a, (long long)blockIdx.x * kWarps + warp, (long long)gridDim.x * kWarps, queues[warp],
+        [&](long long p) { dx0[p] = 0.0; },
+        [&](float xf, float vf, int t, long long p) {
+            Pair pr;
+            if (!cic1d_select(a, xf, vf, t, pr)) return;
+            const double sgn = pr.d > 0.0 ? 1.0 : (pr.d < 0.0 ? -1.0 : 0.0);
+            const double dw = -2.0 * pr.u * sgn / a.hw;
+            const double G0 = 2.0 * ((double)H[pr.b0] - (double)a.target[pr.b0]);
+            const double G1 = 2.0 * ((double)H[pr.b1] - (double)a.target[pr.b1]);
+            atomicAdd(&dx0[p], G0 * (dw * (1.0 - pr.f) - pr.w * nb) + G1 * (dw * pr.f + pr.w * nb));
+        });
+}
+
+pcg_status check_cic1d_args(const float *x0, const float *v, int64_t n, const float *target, int32_t nbins,
+                            int32_t nsteps, double dt, double halfwidth, const float *H, const double *loss) {
+    if (n < 0 || nbins < 1 || nbins > 16384 || nsteps < 1) return PCG_ERR_INVALID_ARG;
+    if (!(halfwidth > 0.0) || !(dt == dt) || !(halfwidth < 1e300) || !(dt < 1e300 && dt > -1e300))
+        return PCG_ERR_INVALID_ARG;
+    if (target == nullptr || H == nullptr || loss == nullptr) return PCG_ERR_INVALID_ARG;
+    if (n > 0 && (x0 == nullptr || v == nullptr)) return PCG_ERR_INVALID_ARG;
+    return PCG_OK;
+}
+
+Cic1dArgs make_args(const float *x0, const float *v, int64_t n, const float *target, int32_t nbins,
+                    int32_t nsteps, double dt, double halfwidth) {
+    Cic1dArgs a;
+    a.x0 = x0;
+    a.v = v;
+    a.n = (long long)n;
+    a.target = target;
+    a.nbins = nbins;
+    a.nsteps = nsteps;
+    a.dt = dt;
+    a.hw = halfwidth;
+    a.dt32 = (float)dt;
+    a.hw32 = (float)halfwidth;
+    a.inv_t32 = 1.0f / (float)nsteps;
+    return a;
+}
+
+// CTAs of a full grid for the large-N kernels: enough to cover the 32-particle
+// chunks, at most what is resident on all SMs at once.
+int full_grid(const void *kernel, size_t smem, long long n) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const long long need = (n + kThreads - 1) / kThreads;
+    const long long cap = (long long)num_sms() * per_sm;
+    return (int)(need < cap ? (need < 1 ? 1 : need) : cap);
+}
+
+pcg_status cic1d_forward(const Cic1dArgs &a, float *H, double *loss, cudaStream_t s) {
+    const size_t smem = (size_t)a.nbins * sizeof(float);
+    // the shared histogram plus the static queues can exceed the 48 KB default
+    static const bool opted_in = [] {
+        const int max_dyn = 16384 * (int)sizeof(float);
+        return cudaFuncSetAttribute(cic1d_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    max_dyn) == cudaSuccess &&
+               cudaFuncSetAttribute(cic1d_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    max_dyn) == cudaSuccess;
+    }();
+    if (!opted_in) return PCG_ERR_CUDA;
+    if (a.n <= kClusterMaxN) {
+        prof::Mark mk("cic1d", s);
+        cic1d_cluster_kernel<<<kCtas, kThreads, smem, s>>>(a, H, loss);
+        return launch_status();
+    }
+    prof::Mark mk("cic1d", s);
+    PCG_CHECK_CUDA(cudaMemsetAsync(H, 0, (size_t)a.nbins * sizeof(float), s));
+    const int grid = full_grid((const void *)cic1d_hist_kernel, smem, a.n);
+    cic1d_hist_kernel<<<grid, kThreads, smem, s>>>(a, H);
+    PCG_CHECK_CUDA(cudaGetLastError());
+    cic1d_loss_kernel<<<1, kThreads, 0, s>>>(H, a.target, a.nbins, loss);
+    return launch_status();
 }
 
 }  // namespace
@@ -125,16 +353,25 @@ extern "C" pcg_status pcg_deposit_cic1d(const float *x0, const float *v, int64_t
                                         double dt, double halfwidth, float *H, double *loss,
                                         void *stream) {
     using namespace pcg;
-    if (n < 0 || nbins < 1 || nbins > 16384 || nsteps < 1) return PCG_ERR_INVALID_ARG;
-    if (!(halfwidth > 0.0) || !(dt == dt) || !(halfwidth < 1e300)) return PCG_ERR_INVALID_ARG;
-    if (target == nullptr || H == nullptr || loss == nullptr) return PCG_ERR_INVALID_ARG;
-    if (n > 0 && (x0 == nullptr || v == nullptr)) return PCG_ERR_INVALID_ARG;
-    const size_t smem = (size_t)nbins * sizeof(float);
-    if (smem > 48 * 1024)
-        PCG_CHECK_CUDA(cudaFuncSetAttribute(cic1d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)smem));
-    prof::Mark mk("cic1d", as_stream(stream));
-    cic1d_kernel<<<kCtas, kThreads, smem, as_stream(stream)>>>(x0, v, (long long)n, target, nbins,
-                                                              nsteps, dt, halfwidth, H, loss);
+    const pcg_status st = check_cic1d_args(x0, v, n, target, nbins, nsteps, dt, halfwidth, H, loss);
+    if (st != PCG_OK) return st;
+    return cic1d_forward(make_args(x0, v, n, target, nbins, nsteps, dt, halfwidth), H, loss, as_stream(stream));
+}
+
+extern "C" pcg_status pcg_deposit_cic1d_grad(const float *x0, const float *v, int64_t n,
+                                             const float *target, int32_t nbins, int32_t nsteps,
+                                             double dt, double halfwidth, float *H, double *loss,
+                                             double *dx0, void *stream) {
+    using namespace pcg;
+    pcg_status st = check_cic1d_args(x0, v, n, target, nbins, nsteps, dt, halfwidth, H, loss);
+    if (st != PCG_OK) return st;
+    if (n > 0 && dx0 == nullptr) return PCG_ERR_INVALID_ARG;
+    const Cic1dArgs a = make_args(x0, v, n, target, nbins, nsteps, dt, halfwidth);
+    const cudaStream_t s = as_stream(stream);
+    st = cic1d_forward(a, H, loss, s);
+    if (st != PCG_OK || n == 0) return st;
+    prof::Mark mk("cic1d_grad", s);
+    const int grid = full_grid((const void *)cic1d_grad_kernel, 0, a.n);
+    cic1d_grad_kernel<<<grid, kThreads, 0, s>>>(a, H, dx0);
     return launch_status();
 }

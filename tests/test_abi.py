@@ -27,7 +27,7 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     names = declared_symbols()
-    for want in ("pcg_deposit_cic1d", "pcg_tile_sort", "pcg_deposit_current", "pcg_assemble_mass_matrix"):
+    for want in ("pcg_deposit_cic1d", "pcg_deposit_cic1d_grad", "pcg_tile_sort", "pcg_deposit_current", "pcg_assemble_mass_matrix"):
         assert want in names
 
 
@@ -65,6 +65,17 @@ def test_cic1d_rejects_bad_arguments(lib):
     assert lib.pcg_deposit_cic1d(vp, vp, 10, vp, 1024, 50, 0.01, 0.0, vp, vp, None) == 1
     assert lib.pcg_deposit_cic1d(vp, vp, 10, vp, 1024, 50, 0.01, 0.005, None, vp, None) == 1
     assert lib.pcg_deposit_cic1d(vp, vp, -1, vp, 1024, 50, 0.01, 0.005, vp, vp, None) == 1
+
+
+def test_cic1d_grad_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p(16)
+    f = lib.pcg_deposit_cic1d_grad
+    assert f(vp, vp, 10, vp, 0, 50, 0.01, 0.005, vp, vp, vp, None) == 1
+    assert f(vp, vp, 10, vp, 1024, 0, 0.01, 0.005, vp, vp, vp, None) == 1
+    assert f(vp, vp, 10, vp, 1024, 50, 0.01, -1.0, vp, vp, vp, None) == 1
+    assert f(vp, vp, 10, vp, 1024, 50, float("nan"), 0.005, vp, vp, vp, None) == 1
+    assert f(vp, vp, 10, vp, 1024, 50, 0.01, 0.005, vp, vp, None, None) == 1  # no dx0
+    assert f(vp, vp, 10, vp, 1024, 50, 0.01, 0.005, vp, None, vp, None) == 1  # no loss
 
 
 def test_workspace_queries(lib):

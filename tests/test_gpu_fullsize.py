@@ -118,3 +118,19 @@ def test_mass3d_64():
                                        [o[idx] for o in d["omega"]])
             box = _box_index(grid, lo, hi)
             assert rel_frobenius(M[box], Mr[box]) <= MASS_TOL, (precision, lo)
+
+
+def test_cic1d_grad_ten_million():
+    """The gradient at N = 10^7 (the size the pages time it at), checked whole."""
+    pcg = need_gpu()
+    d = synth.cic1d(n=10_000_000, seed=1003)
+    H, L, g = pcg.deposit_cic1d_grad(dev(d["x0"]), dev(d["v"]), dev(d["target"]), d["nsteps"], d["dt"],
+                                     d["halfwidth"])
+    gr, Hr, Lr, nsel = oracle.cic1d_grad(d["x0"], d["v"], d["target"], d["nbins"], d["nsteps"], d["dt"],
+                                         d["halfwidth"])
+    H, g = host(H), host(g)
+    assert np.abs(H - Hr).max() <= DEPOSIT_TOL * np.abs(Hr).max()
+    assert abs(float(host(L)[0]) - Lr) <= 1e-5 * Lr
+    assert np.abs(g - gr).max() <= DEPOSIT_TOL * np.abs(gr).max()
+    assert np.array_equal(g == 0.0, gr == 0.0)
+    assert nsel > 4_000_000
