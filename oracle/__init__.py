@@ -62,6 +62,8 @@ def _load():
             lib.oracle_axis_support.argtypes = [i32, dbl, vp, vp]
             lib.oracle_deposit_current.restype = i64
             lib.oracle_deposit_current.argtypes = [i32, vp, i32, i64, vp, vp, vp, vp]
+            lib.oracle_deposit_zigzag.restype = i64
+            lib.oracle_deposit_zigzag.argtypes = [vp, i64, vp, vp, vp, dbl, vp]
             lib.oracle_alpha.restype = None
             lib.oracle_alpha.argtypes = [vp, vp]
             lib.oracle_mass_matrix.restype = i64
@@ -145,6 +147,23 @@ def deposit_current(grid, order, pos, vel, q):
     posp = _ptr_array(pos + [pos[0]] * (3 - dim))
     velp = _ptr_array(vel)
     ninv = lib.oracle_deposit_current(dim, _ptr(g), int(order), n, posp, velp, _ptr(q), _ptr(J))
+    return J.reshape((3,) + tuple(reversed(grid))), int(ninv)
+
+
+def deposit_zigzag(grid, pos_prev, pos, q, dt):
+    """Charge-conserving zigzag current (Umeda et al. 2003; the O == 0 deposit of
+    "Tiled current deposit", "Halo sizing") of the moves pos_prev -> pos on a 3D
+    periodic grid.  Returns (J float64[3, Nz, Ny, Nx], n_invalid); J[c] lives on
+    the edges from each node towards +e_c."""
+    lib = _load()
+    assert len(grid) == 3
+    pp = [_f32(a) for a in pos_prev]
+    pc = [_f32(a) for a in pos]
+    q = _f32(q)
+    g = np.array(grid, dtype=np.int32)
+    J = np.zeros(3 * int(np.prod(grid)), dtype=np.float64)
+    ninv = lib.oracle_deposit_zigzag(_ptr(g), q.size, _ptr_array(pp), _ptr_array(pc), _ptr(q), float(dt),
+                                     _ptr(J))
     return J.reshape((3,) + tuple(reversed(grid))), int(ninv)
 
 

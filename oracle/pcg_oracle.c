@@ -20,7 +20,8 @@
  *    shape, TSC base-offset rule), Sec. 3.4 (offset-indexed stencil storage).
  *  - "Tiled current deposit" (Entity wiki), sections "How a tile deposit runs"
  *    and "The tile-based spatial sort": tile counts ceil(n/T) per axis, tile
- *    key, tile_offsets prefix sum.
+ *    key, tile_offsets prefix sum; section "Halo sizing" names the O == 0
+ *    zigzag deposit, whose scheme is the published one of Umeda et al. (2003).
  *
  * Parity pins: every function here is pinned by the CPU tests against brute
  * force, closed forms or invariants (see tests/test_oracle_pins.py).
@@ -224,6 +225,107 @@ int64_t oracle_deposit_current(int32_t dim, const int32_t *grid, int32_t order,
                 }
             }
         }
+    }
+    return n_invalid;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Charge-conserving zigzag current deposit                                  */
+/* ------------------------------------------------------------------------ */
+/*
+ * The O == 0 deposit of "Tiled current deposit" (Entity wiki), section "Halo
+ * sizing": it writes at most 2 cells above min(i, i_prev).  The page names the
+ * scheme without defining it; this is the zigzag scheme of Umeda, Omura,
+ * Tominaga & Matsumoto, Comput. Phys. Commun. 156 (2003) 73, for unit cells:
+ *
+ * per axis, with cells i1 = floor(x1), i2 = floor(x2) (|i2 - i1| <= 1),
+ *   relay  xr = min(min(i1, i2) + 1, max(max(i1, i2), (x1 + x2) / 2)),
+ *   moves  D1 = xr - x1,  D2 = x2 - xr,  fluxes F_s = q D_s / dt,
+ *   shape  W1 = (x1 + xr) / 2 - i1,  W2 = (xr + x2) / 2 - i2;
+ * segment s (cell (i_s, j_s, k_s)) adds to J^x at the four edges
+ * (i_s + 1/2, j_s + a, k_s + b), a, b in {0, 1}, the flux F_s^x times the
+ * bilinear weight of (W_s^y, W_s^z) averaged along the straight segment:
+ *   w_a(W^y) w_b(W^z) + (a == b ? +1 : -1) D_s^y D_s^z / 12,
+ * w_0(W) = 1 - W, w_1(W) = W; likewise for y and z.  The D D / 12 term is the
+ * exact path average of the product (Villasenor & Buneman); it vanishes when
+ * the segment moves along at most two axes, where the expression is Umeda's.
+ * With rho the CIC charge at the nodes, this J satisfies
+ * (rho(x2) - rho(x1)) / dt + div J = 0 exactly, div taken with backward
+ * differences of the edge currents.
+ *
+ * Layout: J is double[3][ncells]; J[c][(k*Ny + j)*Nx + i] holds the c-current
+ * on the edge from node (i, j, k) towards +e_c.  Periodic on every axis.
+ *
+ * Inputs: pos_prev = x1 and pos = x2, both in [0, N); the move is taken as the
+ * periodic minimum image of the cell difference, so a particle may cross the
+ * periodic boundary.  A particle with a coordinate outside [0, N) (or NaN), or
+ * whose cell changes by more than one along an axis (beyond the scheme's CFL
+ * limit), is skipped and counted.  Returns that count.  grid[mu] >= 3.
+ */
+int64_t oracle_deposit_zigzag(const int32_t *grid, int64_t n, const float *const *pos_prev,
+                              const float *const *pos, const float *q, double dt, double *J) {
+    const int64_t N[3] = {grid[0], grid[1], grid[2]};
+    const int64_t ncells = N[0] * N[1] * N[2];
+    memset(J, 0, sizeof(double) * 3 * (size_t)ncells);
+    int64_t n_invalid = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        int ok = 1;
+        int64_t base[3];        /* lower of the two cells (unwrapped) */
+        int cell[2][3];         /* cell of each segment relative to base: 0 or 1 */
+        double F[2][3], W[2][3], D[2][3];
+        for (int mu = 0; mu < 3 && ok; ++mu) {
+            double x1 = pos_prev[mu][p], x2 = pos[mu][p];
+            if (!in_domain(x1, (int32_t)N[mu]) || !in_domain(x2, (int32_t)N[mu])) {
+                ok = 0;
+                break;
+            }
+            int64_t i1 = (int64_t)floor(x1), i2 = (int64_t)floor(x2);
+            int64_t di = i2 - i1;  /* periodic minimum image */
+            if (2 * di > N[mu]) di -= N[mu];
+            if (2 * di < -N[mu]) di += N[mu];
+            if (di < -1 || di > 1) {
+                ok = 0;
+                break;
+            }
+            int64_t lo = di < 0 ? di : 0;
+            int a = (int)(-lo), b = (int)(di - lo);
+            /* positions relative to the lower cell's low node */
+            double X1 = (double)a + (x1 - (double)i1);
+            double X2 = (double)b + (x2 - (double)i2);
+            double hi = (double)(a > b ? a : b);
+            double xr = fmin(1.0, fmax(hi, 0.5 * (X1 + X2)));
+            base[mu] = i1 + lo;
+            cell[0][mu] = a;
+            cell[1][mu] = b;
+            D[0][mu] = xr - X1;
+            D[1][mu] = X2 - xr;
+            F[0][mu] = (double)q[p] * D[0][mu] / dt;
+            F[1][mu] = (double)q[p] * D[1][mu] / dt;
+            W[0][mu] = 0.5 * (X1 + xr) - (double)a;
+            W[1][mu] = 0.5 * (xr + X2) - (double)b;
+        }
+        if (!ok) {
+            ++n_invalid;
+            continue;
+        }
+        for (int s = 0; s < 2; ++s)
+            for (int c = 0; c < 3; ++c) {
+                int u = (c + 1) % 3, v = (c + 2) % 3; /* the two transverse axes */
+                for (int du = 0; du < 2; ++du)
+                    for (int dv = 0; dv < 2; ++dv) {
+                        int64_t node[3];
+                        for (int mu = 0; mu < 3; ++mu) node[mu] = base[mu] + cell[s][mu];
+                        node[u] += du;
+                        node[v] += dv;
+                        double wu = du ? W[s][u] : 1.0 - W[s][u];
+                        double wv = dv ? W[s][v] : 1.0 - W[s][v];
+                        double avg = D[s][u] * D[s][v] / 12.0;
+                        double w = wu * wv + (du == dv ? avg : -avg);
+                        int64_t g = (mod_floor(node[2], N[2]) * N[1] + mod_floor(node[1], N[1])) * N[0] +
+                                    mod_floor(node[0], N[0]);
+                        J[c * ncells + g] += F[s][c] * w;
+                    }
+            }
     }
     return n_invalid;
 }

@@ -470,3 +470,110 @@ def test_tile_keys_against_bincount(grid, tile):
     counts = np.bincount(k, minlength=total + 1)[:total]
     assert np.array_equal(offs, np.concatenate([[0], np.cumsum(counts)]).astype(np.uint32))
     assert offs[-1] == ok.sum()
+
+
+# ---------------------------------------------------------------------------
+# Charge-conserving zigzag current deposit (the O == 0 deposit named in "Tiled
+# current deposit", "Halo sizing"; scheme of Umeda et al. 2003).  Pins: hand-
+# worked values, the discrete continuity equation against a CIC charge density
+# built here from its definition, the total current, and time reversal.
+# ---------------------------------------------------------------------------
+def _zigzag_moves(grid, n, seed, dmax=0.95):
+    rng = np.random.default_rng(seed)
+    x1 = [synth.to_cell_f32(rng.random(n) * N, N) for N in grid]
+    x2 = [synth.to_cell_f32(a.astype(np.float64) + rng.uniform(-dmax, dmax, n), N) for a, N in zip(x1, grid)]
+    q = rng.choice([-1.0, 1.0, 0.5], n).astype(np.float32)
+    return x1, x2, q
+
+
+def _cic_rho(grid, pos, q):
+    """Charge on the nodes: every particle gives q (1 - f) / q f to the two nodes
+    around it along each axis (the product over axes), periodic."""
+    import itertools
+    rho = np.zeros(tuple(reversed(grid)))
+    for corner in itertools.product((0, 1), repeat=3):
+        w = q.astype(np.float64).copy()
+        idx = []
+        for mu, N in enumerate(grid):
+            x = pos[mu].astype(np.float64)
+            i = np.floor(x)
+            f = x - i
+            w *= f if corner[mu] else 1.0 - f
+            idx.append(((i + corner[mu]) % N).astype(np.int64))
+        np.add.at(rho, (idx[2], idx[1], idx[0]), w)
+    return rho
+
+
+def _div_backward(J):
+    # J[c] on the edge from node g towards +e_c: (div J)_g = sum_c J_c(g) - J_c(g - e_c);
+    # array axes are (z, y, x), so component c differences along axis 2 - c
+    return sum(J[c] - np.roll(J[c], 1, axis=2 - c) for c in range(3))
+
+
+def _golden_zigzag():
+    rows = read_golden("zigzag_worked.txt")
+    grid = tuple(int(v) for v in rows[0][1:])
+    dt = float(rows[1][1])
+    parts, cur = {}, None
+    for r in rows[2:]:
+        if r[0] == "particle":
+            cur = r[1]
+            parts[cur] = ([float(v) for v in r[2:5]], [float(v) for v in r[5:8]], {})
+        else:
+            c, i, j, k, num = (int(v) for v in r[1:])
+            parts[cur][2][(c, k, j, i)] = Fraction(num, 384)
+    return grid, dt, parts
+
+
+@pytest.mark.parametrize("name", ["A", "C", "D", "E"])
+def test_zigzag_worked_examples(name):
+    grid, dt, parts = _golden_zigzag()
+    x1, x2, want = parts[name]
+    J, ninv = oracle.deposit_zigzag(grid, [np.array([v], np.float32) for v in x1],
+                                    [np.array([v], np.float32) for v in x2], np.ones(1, np.float32), dt)
+    assert ninv == 0
+    got = {tuple(int(v) for v in ix): float(J[ix]) for ix in zip(*np.nonzero(J))}
+    assert set(got) == set(want)
+    # thirds (the /12 terms) are not binary fractions: allow the rounding of a few operations
+    for k, v in want.items():
+        assert abs(got[k] - float(v)) <= 4e-16, (k, got[k], v)
+
+
+@pytest.mark.parametrize("grid,dt,seed", [((3, 3, 3), 1.0, 1), ((5, 6, 7), 0.5, 2), ((8, 4, 5), 0.3, 3),
+                                          ((4, 9, 3), 2.0, 4)])
+def test_zigzag_continuity_equation(grid, dt, seed):
+    x1, x2, q = _zigzag_moves(grid, 3000, seed)
+    J, ninv = oracle.deposit_zigzag(grid, x1, x2, q, dt)
+    assert ninv == 0
+    res = (_cic_rho(grid, x2, q) - _cic_rho(grid, x1, q)) / dt + _div_backward(J)
+    assert np.abs(res).max() <= 1e-11 * max(1.0, np.abs(J).max())
+    # and the current is not trivially zero
+    assert np.abs(J).max() > 1.0
+
+
+def test_zigzag_total_current_and_time_reversal():
+    grid, dt = (6, 5, 7), 0.25
+    x1, x2, q = _zigzag_moves(grid, 2000, 11)
+    J, _ = oracle.deposit_zigzag(grid, x1, x2, q, dt)
+    for c, N in enumerate(grid):
+        d = x2[c].astype(np.float64) - x1[c].astype(np.float64)
+        d -= N * np.round(d / N)  # the periodic minimum image of the move
+        assert abs(J[c].sum() - np.sum(q * d) / dt) <= 1e-10 * np.abs(q * d / dt).sum()
+    Jr, _ = oracle.deposit_zigzag(grid, x2, x1, q, dt)
+    assert np.abs(J + Jr).max() <= 1e-12 * np.abs(J).max()
+
+
+def test_zigzag_invalid_moves_skipped_and_counted():
+    grid, dt = (6, 6, 6), 1.0
+    x1, x2, q = _zigzag_moves(grid, 500, 12)
+    J_ok, _ = oracle.deposit_zigzag(grid, x1, x2, q, dt)
+    bad1 = [np.array([1.5, 0.5, 2.5, 3.5], np.float32), np.array([1.5, 0.5, 2.5, np.nan], np.float32),
+            np.array([1.5, 0.5, 2.5, 1.0], np.float32)]
+    bad2 = [np.array([3.5, 0.5, 2.5, 3.5], np.float32),   # two cells along x
+            np.array([1.5, 6.0, 2.5, 1.0], np.float32),   # y outside [0, 6)
+            np.array([1.5, 0.5, -0.25, 1.0], np.float32)]  # z below 0
+    a = [np.concatenate([u, v]) for u, v in zip(x1, bad1)]
+    b = [np.concatenate([u, v]) for u, v in zip(x2, bad2)]
+    J, ninv = oracle.deposit_zigzag(grid, a, b, np.concatenate([q, np.ones(4, np.float32)]), dt)
+    assert ninv == 4
+    assert np.array_equal(J, J_ok)
