@@ -312,6 +312,59 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
     return res
 
 
+def zigzag_workload(pcg, d, steps, warmup, dist, peaks, traffic):
+    """Time sort (keyed on the previous positions) + tiled charge-conserving
+    zigzag deposit on a 3D move workload; returns a dict."""
+    import torch
+    grid, n = d["grid"], d["n"]
+    stream = torch.cuda.current_stream()
+    dev = lambda a: torch.from_numpy(a).cuda()
+    prev = [dev(a) for a in d["pos_prev"]]
+    pos = [dev(a) for a in d["pos"]]
+    q = dev(d["q"])
+    payload = prev + pos + [q]
+    out = [torch.empty_like(p) for p in payload]
+    nt = pcg.n_tiles(grid, d["tile"])
+    offs = torch.empty(nt + 1, dtype=torch.int32, device="cuda")
+    J = torch.empty((3,) + tuple(reversed(grid)), dtype=torch.float32, device="cuda")
+    ws_s = torch.empty(max(pcg.tile_sort_workspace_size(grid, d["tile"], n, len(payload)), 256), dtype=torch.uint8,
+                       device="cuda")
+    ws_d = torch.empty(max(pcg.deposit_current_workspace_size(grid, d["tile"], n), 256), dtype=torch.uint8,
+                       device="cuda")
+    stats = pcg.new_stats()
+
+    def step():
+        pcg.tile_sort(grid, d["tile"], prev, payload, out=out, tile_offsets=offs, workspace=ws_s)
+        pcg.deposit_zigzag(grid, out[0:3], out[3:6], out[6], d["dt"], tile_offsets=offs, tile=d["tile"], J=J,
+                           stats=stats, workspace=ws_d)
+
+    step()
+    torch.cuda.synchronize()
+    st = pcg.read_stats(stats)
+    ms = time_steps(step, steps, warmup, dist, stream, pcg=pcg)
+    timed = pcg.profile_collect()
+    ms = dist.max(ms)
+    nf = 7  # payload fields: previous and current positions, q
+    alg = {
+        "deposit_zigzag": n * 4 * nf + 12 * int(np.prod(grid)),
+        "sort_count": n * 12,
+        "sort_partition1": n * (4 * nf + 4 * (nf + 1)),
+        "sort_partition2": n * (4 * (nf + 1) + 4 * nf),
+        "sort_partition": n * 2 * 4 * nf,
+        "sort_scatter": n * 2 * 4 * nf,
+    }
+    kern = {name: roofline_entry(name, timed, b, peaks["hbm_gbs"], traffic, n)
+            for name, b in alg.items() if name in timed}
+    res = {"workload": f"zigzag3d {grid[0]}x{grid[1]}x{grid[2]} x {n // int(np.prod(grid))} ppc, "
+                       "charge-conserving, sorted by previous position", "particles": n,
+           "value": round(n * steps * dist.world / (ms * 1e-3) / 1e6, 1), "unit": UNIT,
+           "ms_per_step": round(ms / steps, 4), "kernels": kern, "escaped_per_step": st["n_escaped"],
+           "invalid": st["n_invalid"], "gpu_launches": sum(v[0] for v in timed.values())}
+    del prev, pos, q, payload, out, J, ws_s, ws_d
+    torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline_current(d, budget_s=12.0):
     """The fp64 oracle as it stands, single-threaded, on a bounded random sample."""
     import oracle
@@ -458,6 +511,9 @@ def run_gpu(args):
                                  "stencil_updates_per_s": r4.get("stencil_updates_per_s")}
         del d4
         wl["mass3d_64"] = mass_workload(pcg, ks, kw, dist, peaks, traffic)
+        d5 = synth.zigzag3d()
+        wl["zigzag3d_256"] = zigzag_workload(pcg, d5, ks, kw, dist, peaks, traffic)
+        del d5
         line["workloads"] = wl
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
@@ -478,6 +534,9 @@ def run_only(args):
         out = mass_workload(pcg, args.steps, args.warmup, dist, peaks, traffic, edge=args.mass_grid)
     elif args.only == "cic1d":
         out = cic1d_workload(pcg, args.steps, args.warmup, dist)
+    elif args.only == "zigzag":
+        out = zigzag_workload(pcg, synth.zigzag3d(grid=(args.zz_grid,) * 3), args.steps, args.warmup, dist, peaks,
+                              traffic)
     else:
         d = synth.quad3d_bump() if args.only == "quad" else synth.cic2d()
         out = current_workload(pcg, d, args.steps, args.warmup, dist, peaks, traffic)
@@ -533,9 +592,10 @@ def main():
     ap.add_argument("--grid", type=int, default=256, help="edge of the headline workload's grid (256 = full size)")
     ap.add_argument("--main-only", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["mass", "quad", "cic2d", "cic1d"], default=None,
+    ap.add_argument("--only", choices=["mass", "quad", "cic2d", "cic1d", "zigzag"], default=None,
                     help="time one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--mass-grid", type=int, default=64, help="edge of the mass-matrix grid")
+    ap.add_argument("--zz-grid", type=int, default=256, help="edge of the zigzag grid (--only zigzag)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

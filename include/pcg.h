@@ -246,6 +246,54 @@ PCG_API pcg_status pcg_deposit_current_noalloc(int32_t dim, const int32_t *grid,
                                                pcg_stats *stats, void *stream);
 
 /* -------------------------------------------------------------------------
+ * Charge-conserving zigzag current deposit, 3D.
+ * Named by "Tiled current deposit" (Entity wiki), section "Halo sizing" (the
+ * O == 0 zigzag deposit, writing at most 2 cells above min(i, i_prev)) and run
+ * the way "How a tile deposit runs" and "Correctness is independent of the
+ * halo" describe; the scheme is Umeda, Omura, Tominaga & Matsumoto, Comput.
+ * Phys. Commun. 156 (2003) 73.  Per axis, cells i1 = floor(x1), i2 = floor(x2):
+ *   xr = min(min(i1,i2) + 1, max(max(i1,i2), (x1 + x2)/2)),
+ *   D1 = xr - x1, D2 = x2 - xr, F_s = q D_s / dt,
+ *   W1 = (x1 + xr)/2 - i1, W2 = (xr + x2)/2 - i2;
+ * segment s adds F_s^c (w_a(W_s^u) w_b(W_s^v) + (a == b ? 1 : -1) D_s^u D_s^v / 12)
+ * to the c-edge starting at its cell + a e_u + b e_v (u, v the transverse axes,
+ * w_0(W) = 1 - W, w_1(W) = W).  The D D / 12 term (the weight averaged along
+ * the straight segment) makes (rho(x2) - rho(x1)) / dt + div J = 0 exact for
+ * the CIC charge rho; it is zero when a segment moves along at most two axes.
+ *
+ * Output layout: J float[3][Nz][Ny][Nx]; J[c] at node (i, j, k) is the
+ * c-current on the edge from that node towards +e_c.  Periodic on every axis.
+ *
+ *   grid       HOST int32[3], each in [3, 2^20].
+ *   tile       8 (with tile_offsets); ignored when tile_offsets is NULL.
+ *   n          number of particles, 0 <= n < 2^32 - 1.
+ *   pos_prev, pos  HOST arrays of 3 device float[n]: the positions before and
+ *              after the move, both in [0, N).  The move is the periodic
+ *              minimum image of the cell change, so a particle may cross the
+ *              periodic boundary.
+ *   q          device float[n]; dt > 0.
+ *   tile_offsets  NULL (flat: every particle through global reductions) or the
+ *              output of pcg_tile_sort with tile 8 keyed on pos_prev and with
+ *              pos_prev, pos and q among its payload.  Particles whose 3x3x3
+ *              footprint leaves their tile's window (tile + 2 cells per side)
+ *              take the escape valve (stats->n_escaped).
+ *   J          device float[3 * ncells], 16-byte aligned, output (overwritten).
+ *   stats      device pcg_stats or NULL: n_invalid counts particles with a
+ *              coordinate outside [0, N) or NaN, or whose cell changes by more
+ *              than one along an axis (beyond the scheme's CFL limit); they are
+ *              skipped.
+ *   workspace  pcg_deposit_current_workspace_size(3, grid, 8, n) bytes when
+ *              tiled, else may be NULL.
+ * Launches: 2 (zero J + chunk map, deposit).  Errors: PCG_ERR_INVALID_ARG for
+ * bad sizes, pointers or dt; PCG_ERR_UNSUPPORTED for a tile other than 8.
+ */
+PCG_API pcg_status pcg_deposit_zigzag(const int32_t *grid, int32_t tile, int64_t n,
+                                      const float *const *pos_prev, const float *const *pos,
+                                      const float *q, double dt, const uint32_t *tile_offsets,
+                                      float *J, pcg_stats *stats, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* -------------------------------------------------------------------------
  * ECSIM block mass matrix with first-order (CIC) B-splines.
  * Defined by Pennati & Markidis, Sec. 2.1, Eqs. (4)-(6):
  *   M^{ij}_{g g'} = sum_p s_p^{ij} W_pg W_pg',  s_p = w_p alpha_p,

@@ -7,7 +7,8 @@ provides device memory and streams.  Outputs not supplied by the caller are
 allocated with torch; workspaces likewise.
 
 Entry points (same names as the C ABI without the ``pcg_`` prefix):
-  deposit_cic1d, deposit_cic1d_grad, tile_sort, deposit_current, assemble_mass_matrix,
+  deposit_cic1d, deposit_cic1d_grad, tile_sort, deposit_current, deposit_zigzag,
+  assemble_mass_matrix,
   plus the *_workspace_size queries and stats helpers.
 """
 from __future__ import annotations
@@ -21,7 +22,7 @@ from ._lib import PcgError, check
 
 __all__ = [
     "PcgError", "version", "deposit_cic1d", "deposit_cic1d_grad", "tile_sort", "tile_sort_workspace_size",
-    "deposit_current", "deposit_current_workspace_size", "assemble_mass_matrix",
+    "deposit_current", "deposit_current_workspace_size", "deposit_zigzag", "assemble_mass_matrix",
     "assemble_mass_matrix_workspace_size", "new_stats", "read_stats", "n_tiles",
     "profile_enable", "profile_collect",
 ]
@@ -202,6 +203,33 @@ def deposit_current(grid, order, pos, vel, q, tile_offsets=None, tile=8, halo=1,
                                          _ptr(tile_offsets), _ptr(J), _ptr(stats), _ptr(ws),
                                          _ws_bytes(ws), _stream(stream))
     check(st, "pcg_deposit_current")
+    return J
+
+
+def deposit_zigzag(grid, pos_prev, pos, q, dt, tile_offsets=None, tile=8, J=None, stats=None, workspace=None,
+                   stream=None):
+    """Charge-conserving zigzag current of the moves pos_prev -> pos
+    (float32[3, Nz, Ny, Nx], J[c] on the edges from each node towards +e_c);
+    tiled when tile_offsets (a tile sort keyed on pos_prev) is given."""
+    assert len(grid) == 3
+    n = q.numel()
+    for i, t in enumerate(pos_prev):
+        _dev(t, torch.float32, f"pos_prev[{i}]")
+    for i, t in enumerate(pos):
+        _dev(t, torch.float32, f"pos[{i}]")
+    _dev(q, torch.float32, "q")
+    dev = q.device
+    shape = (3,) + tuple(int(N) for N in reversed(grid))
+    J = torch.empty(shape, dtype=torch.float32, device=dev) if J is None else _dev(J, torch.float32, "J")
+    if tile_offsets is not None:
+        _dev(tile_offsets, None, "tile_offsets")
+        ws = _workspace(deposit_current_workspace_size(grid, tile, n), dev, workspace)
+    else:
+        ws = workspace
+    st = _lib.load().pcg_deposit_zigzag(_grid_arr(grid), int(tile), n, _ptr_arr(pos_prev, 3), _ptr_arr(pos, 3),
+                                        _ptr(q), float(dt), _ptr(tile_offsets), _ptr(J), _ptr(stats), _ptr(ws),
+                                        _ws_bytes(ws), _stream(stream))
+    check(st, "pcg_deposit_zigzag")
     return J
 
 

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(256)
     warp_add_u64(ctr.n_invalid, n_inv);
 }
 
+}  // namespace
+
 // Particles per CTA of the tiled kernel: a power of two in [1024, 16384], about
 // 16 chunks per SM so that the last wave is short.
 long long chunk_for(long long n) {
@@ -82,7 +84,22 @@ bool geom_from(int32_t dim, const int32_t *grid, int tile, Geom *g) {
     return true;
 }
 
-}  // namespace
+pcg_status launch_prep(float *J, const Geom &g, const uint32_t *tile_offsets, long long n, long long chunk,
+                       unsigned *chunk_tile, unsigned *flags, cudaStream_t s) {
+    const long long nchunks = (n + chunk - 1) / chunk;
+    const size_t nJ = 3 * (size_t)g.ncells;
+    size_t work = nJ / 4 > (size_t)nchunks ? nJ / 4 : (size_t)nchunks;
+    if (tile_offsets != nullptr && (size_t)g.n_tiles > work) work = g.n_tiles;
+    size_t blocks = (work + 255) / 256;
+    const size_t cap = (size_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    prof::Mark mk("deposit_prep", s);
+    prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(J, nJ, tile_offsets, g.n_tiles, n, chunk, chunk_tile, nchunks,
+                                                flags);
+    return launch_status();
+}
+
 }  // namespace pcg
 
 extern "C" pcg_status pcg_deposit_current_workspace_size(int32_t dim, const int32_t *grid,
@@ -138,19 +155,9 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
     Counters ctr{stats ? &stats->n_escaped : nullptr, stats ? &stats->n_invalid : nullptr,
                  stats ? &stats->error_flags : nullptr};
     unsigned *chunk_tile = static_cast<unsigned *>(workspace);
-    const size_t nJ = 3 * (size_t)g.ncells;
     {
-        size_t work = nJ / 4 > (size_t)nchunks ? nJ / 4 : (size_t)nchunks;
-        if (tiled && (size_t)g.n_tiles > work) work = g.n_tiles;
-        size_t blocks = (work + 255) / 256;
-        const size_t cap = (size_t)num_sms() * 8;
-        if (blocks > cap) blocks = cap;
-        if (blocks < 1) blocks = 1;
-        prof::Mark mk("deposit_prep", s);
-        prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(J, nJ, tiled ? tile_offsets : nullptr,
-                                                    g.n_tiles, n, chunk, chunk_tile, nchunks,
-                                                    ctr.flags);
-        PCG_CHECK_LAUNCH();
+        const pcg_status st = launch_prep(J, g, tiled ? tile_offsets : nullptr, n, chunk, chunk_tile, ctr.flags, s);
+        if (st != PCG_OK) return st;
     }
     if (n == 0) return PCG_OK;
     if (!tiled) {

@@ -119,6 +119,14 @@ __device__ __forceinline__ int local_index(int f, int origin, int N) {
 
 }  // namespace dep
 
+// host-side helpers shared by the deposit entry points (deposit.cu)
+long long chunk_for(long long n);
+bool geom_from(int32_t dim, const int32_t *grid, int tile, dep::Geom *g);
+// zero J (3 * ncells floats, 16-byte aligned), and with tile_offsets given,
+// map every chunk of the sorted array to its first tile and check the layout
+pcg_status launch_prep(float *J, const dep::Geom &g, const uint32_t *tile_offsets, long long n, long long chunk,
+                       unsigned *chunk_tile, unsigned *flags, cudaStream_t s);
+
 // host-side dispatchers (deposit_2d.cu / deposit_3d.cu)
 pcg_status deposit_tiled_2d(int order, int tile, int halo, const dep::Geom &g, long long n,
                             const dep::Particles &P, const uint32_t *offs, float *J,

@@ -22,6 +22,11 @@ small cases with the same recipe as the full-size workloads:
                  rho = rho0 + rho1 exp(-r^2 / (2 * 16^2)), r the periodic
                  distance to the box centre, rho0 + rho1 = 10 x mean;
                  v ~ N(0, 0.1^2).                               (seed 1004)
+  zigzag3d       3D periodic grid, exactly ppc per cell at the previous
+                 positions, shuffled; v ~ N(0, 0.05^2) clipped to |v dt| <= 0.95;
+                 pos = wrap(pos_prev + v dt); optionally a subset moved by whole
+                 tiles so that stale sort keys leave them outside their tile.
+                                                               (seed 1006)
   mass3d         3D periodic grid, exactly ppc per cell, shuffled;
                  w ~ U[0.5, 1.5]; b a random unit vector, beta ~ U(0, 1),
                  omega = beta b.                                (seed 1005)
@@ -124,6 +129,37 @@ def cic3d_drift(grid=(256, 256, 256), ppc=16, sigma_v=0.05, dt=1.0, displaced_fr
         del x64
     return dict(grid=tuple(grid), order=1, tile=tile, halo=halo, n=n,
                 key_pos=xs, pos=pos, vel=vel, q=_halves(n), displaced=idx)
+
+
+def zigzag3d(grid=(256, 256, 256), ppc=16, sigma_v=0.05, dt=1.0, vmax=0.95, escaped_frac=0.0, seed=1006,
+             tile=8):
+    """Moves pos_prev -> pos for the charge-conserving deposit: exactly ppc
+    particles per cell at pos_prev (the sort-time positions), v ~ N(0, sigma^2)
+    per component clipped to |v| dt <= vmax (< 1 cell: the scheme's CFL limit),
+    pos = wrap(pos_prev + v dt).  escaped_frac of the particles are first moved
+    by a further whole number of tiles (1..3 per axis) in both pos_prev and pos,
+    so that they sit far outside the tile they are sorted under only when the
+    caller sorts with stale keys (key_pos_stale)."""
+    rng = _rng(seed)
+    n, coords = _cells_uniform(rng, grid, ppc)
+    prev = [_inside_cell_f32(c, rng.random(n)) for c in coords]
+    del coords
+    vel = _maxwellian(rng, n, sigma_v)
+    pos = []
+    for mu, N in enumerate(grid):
+        d = np.clip(vel[mu].astype(np.float64) * dt, -vmax, vmax)
+        pos.append(to_cell_f32(prev[mu].astype(np.float64) + d, N))
+    k = int(round(escaped_frac * n))
+    stale = prev
+    if k:
+        idx = rng.choice(n, size=k, replace=False)
+        stale = [a.copy() for a in prev]
+        for mu, N in enumerate(grid):
+            shift = rng.integers(1, 4, size=k) * tile * rng.choice([-1, 1], size=k)
+            prev[mu][idx] = to_cell_f32(prev[mu][idx].astype(np.float64) + shift, N)
+            pos[mu][idx] = to_cell_f32(pos[mu][idx].astype(np.float64) + shift, N)
+    return dict(grid=tuple(grid), tile=tile, n=n, dt=dt, pos_prev=prev, pos=pos, q=_halves(n),
+                key_pos=prev, key_pos_stale=stale)
 
 
 def bump_density(grid, mean=32.0, peak=320.0, sigma=16.0):

@@ -27,7 +27,7 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     names = declared_symbols()
-    for want in ("pcg_deposit_cic1d", "pcg_deposit_cic1d_grad", "pcg_tile_sort", "pcg_deposit_current", "pcg_assemble_mass_matrix"):
+    for want in ("pcg_deposit_cic1d", "pcg_deposit_cic1d_grad", "pcg_deposit_zigzag", "pcg_tile_sort", "pcg_deposit_current", "pcg_assemble_mass_matrix"):
         assert want in names
 
 
@@ -65,6 +65,21 @@ def test_cic1d_rejects_bad_arguments(lib):
     assert lib.pcg_deposit_cic1d(vp, vp, 10, vp, 1024, 50, 0.01, 0.0, vp, vp, None) == 1
     assert lib.pcg_deposit_cic1d(vp, vp, 10, vp, 1024, 50, 0.01, 0.005, None, vp, None) == 1
     assert lib.pcg_deposit_cic1d(vp, vp, -1, vp, 1024, 50, 0.01, 0.005, vp, vp, None) == 1
+
+
+def test_zigzag_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p(4096)
+    arr = (ctypes.c_void_p * 3)(4096, 4096, 4096)
+    f = lib.pcg_deposit_zigzag
+    g = _grid(8, 8, 8)
+    assert f(_grid(8, 2, 8), 8, 10, arr, arr, vp, 1.0, None, vp, None, None, 0, None) == 1  # grid < 3
+    assert f(g, 8, 10, arr, arr, vp, 0.0, None, vp, None, None, 0, None) == 1              # dt <= 0
+    assert f(g, 8, 10, arr, arr, vp, float("nan"), None, vp, None, None, 0, None) == 1
+    assert f(g, 8, 10, None, arr, vp, 1.0, None, vp, None, None, 0, None) == 1             # no pos_prev
+    assert f(g, 8, 10, arr, arr, vp, 1.0, None, None, None, None, 0, None) == 1            # no J
+    assert f(g, 8, 10, arr, arr, vp, 1.0, None, ctypes.c_void_p(4100), None, None, 0, None) == 1  # J unaligned
+    assert f(g, 4, 10, arr, arr, vp, 1.0, vp, vp, None, vp, 1 << 20, None) == 3            # tile 4: unsupported
+    assert f(g, 8, 10, arr, arr, vp, 1.0, vp, vp, None, None, 0, None) == 2                # tiled, no workspace
 
 
 def test_cic1d_grad_rejects_bad_arguments(lib):

@@ -134,3 +134,35 @@ def test_cic1d_grad_ten_million():
     assert np.abs(g - gr).max() <= DEPOSIT_TOL * np.abs(gr).max()
     assert np.array_equal(g == 0.0, gr == 0.0)
     assert nsel > 4_000_000
+
+
+def test_zigzag3d_256():
+    """Charge-conserving zigzag deposit on 256^3 x 16 ppc moves, in the bench's
+    launch configuration: sampled boxes against the oracle, and the total
+    current of every component against sum_p q (x - x_prev) / dt."""
+    pcg = need_gpu()
+    d = synth.zigzag3d()
+    grid = d["grid"]
+    pp = [dev(a) for a in d["pos_prev"]]
+    pc = [dev(a) for a in d["pos"]]
+    qd = dev(d["q"])
+    out, offs = pcg.tile_sort(grid, 8, pp, pp + pc + [qd])
+    del pc, qd
+    stats = pcg.new_stats()
+    J = host(pcg.deposit_zigzag(grid, out[0:3], out[3:6], out[6], d["dt"], tile_offsets=offs, stats=stats))
+    del out, offs, pp
+    st = stats_dict(stats)
+    assert st["n_invalid"] == 0 and st["n_escaped"] == 0
+    for lo, hi in [((0, 0, 0), (6, 6, 6)), ((250, 120, 60), (256, 128, 67)), ((128, 255, 3), (134, 258, 9))]:
+        idx = _near_box(d["pos"], grid, lo, hi)
+        Jr, _ = oracle.deposit_zigzag(grid, [a[idx] for a in d["pos_prev"]], [a[idx] for a in d["pos"]],
+                                      d["q"][idx], d["dt"])
+        box = _box_index(grid, lo, hi)
+        for c in range(3):
+            ref = Jr[c][box]
+            assert np.abs(J[c][box].astype(np.float64) - ref).max() <= DEPOSIT_TOL * np.abs(ref).max(), (lo, c)
+    for c, N in enumerate(grid):
+        dx = d["pos"][c].astype(np.float64) - d["pos_prev"][c].astype(np.float64)
+        dx -= N * np.round(dx / N)
+        qd = d["q"].astype(np.float64) * dx / d["dt"]
+        assert abs(J[c].astype(np.float64).sum() - qd.sum()) <= 1e-6 * np.abs(qd).sum()
