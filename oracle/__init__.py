@@ -62,6 +62,8 @@ def _load():
             lib.oracle_axis_support.argtypes = [i32, dbl, vp, vp]
             lib.oracle_deposit_current.restype = i64
             lib.oracle_deposit_current.argtypes = [i32, vp, i32, i64, vp, vp, vp, vp]
+            lib.oracle_mass_matrix_scalar.restype = i64
+            lib.oracle_mass_matrix_scalar.argtypes = [vp, i64, vp, vp, vp]
             lib.oracle_deposit_zigzag.restype = i64
             lib.oracle_deposit_zigzag.argtypes = [vp, i64, vp, vp, vp, dbl, vp]
             lib.oracle_alpha.restype = None
@@ -188,6 +190,19 @@ def mass_matrix(grid, pos, wq, omega):
     ninv = lib.oracle_mass_matrix(_ptr(g), wq.size, _ptr_array(pos), _ptr(wq),
                                   _ptr_array(omega), _ptr(M))
     return M.reshape(tuple(reversed(grid)) + (27, 3, 3)), int(ninv)
+
+
+def mass_matrix_scalar(grid, pos, w):
+    """Scalar (MPM) mass matrix M (float64[Nz, Ny, Nx, 27]) = sum_p w W_pg W_pg' for
+    CIC shapes (Pennati & Markidis, Sec. 2.1, the scalar case of Eq. (6));
+    returns (M, n_invalid)."""
+    lib = _load()
+    pos = [_f32(p) for p in pos]
+    w = _f32(w)
+    g = np.array(grid, dtype=np.int32)
+    M = np.zeros(int(np.prod(grid)) * 27, dtype=np.float64)
+    ninv = lib.oracle_mass_matrix_scalar(_ptr(g), w.size, _ptr_array(pos), _ptr(w), _ptr(M))
+    return M.reshape(tuple(reversed(grid)) + (27,)), int(ninv)
 
 
 def tile_keys(grid, tile, pos):

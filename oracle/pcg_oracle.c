@@ -396,6 +396,43 @@ int64_t oracle_mass_matrix(const int32_t *grid, int64_t n,
     return n_invalid;
 }
 
+/* Scalar mass matrix (Pennati & Markidis, Sec. 2.1 after Eq. (6): the scalar
+ * case s_p^{ij} = q_p delta^{ij}, e.g. the MPM mass matrix, one component per
+ * node pair): M_{gg'} = sum_p w_p W_pg W_pg' with CIC shapes, stored by stencil
+ * offset as M[g][o], o = (dz+1)*9 + (dy+1)*3 + (dx+1) for g' = g + (dx,dy,dz)
+ * (periodic).  M is double[ncells][27], overwritten.  Returns the number of
+ * particles skipped for a coordinate outside [0, N). */
+int64_t oracle_mass_matrix_scalar(const int32_t *grid, int64_t n, const float *const *pos,
+                                  const float *w, double *M) {
+    int32_t Nx = grid[0], Ny = grid[1], Nz = grid[2];
+    int64_t ncells = (int64_t)Nx * Ny * Nz;
+    memset(M, 0, sizeof(double) * 27 * (size_t)ncells);
+    int64_t n_invalid = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        double x[3] = {pos[0][p], pos[1][p], pos[2][p]};
+        if (!in_domain(x[0], Nx) || !in_domain(x[1], Ny) || !in_domain(x[2], Nz)) {
+            ++n_invalid;
+            continue;
+        }
+        int64_t first[3];
+        double wt[3][3];
+        for (int mu = 0; mu < 3; ++mu) axis_support(1, x[mu], &first[mu], wt[mu]);
+        for (int a = 0; a < 8; ++a) {
+            int ax = a & 1, ay = (a >> 1) & 1, az = (a >> 2) & 1;
+            double Wa = wt[0][ax] * wt[1][ay] * wt[2][az];
+            int64_t g = (mod_floor(first[2] + az, Nz) * Ny + mod_floor(first[1] + ay, Ny)) * Nx
+                        + mod_floor(first[0] + ax, Nx);
+            for (int b = 0; b < 8; ++b) {
+                int bx = b & 1, by = (b >> 1) & 1, bz = (b >> 2) & 1;
+                double Wb = wt[0][bx] * wt[1][by] * wt[2][bz];
+                int o = (bz - az + 1) * 9 + (by - ay + 1) * 3 + (bx - ax + 1);
+                M[(size_t)g * 27 + (size_t)o] += (double)w[p] * Wa * Wb;
+            }
+        }
+    }
+    return n_invalid;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Tile key and tile_offsets ("Tiled current deposit", tile-based sort)      */
 /* ------------------------------------------------------------------------ */

@@ -395,6 +395,42 @@ def test_mass_matrix_dense_product(grid):
     assert np.abs(got - want).max() <= 1e-12 * np.abs(want).max()
 
 
+@pytest.mark.parametrize("grid", [(3, 4, 5), (5, 3, 4)])
+def test_scalar_mass_matrix_dense_product(grid):
+    """M = W diag(w) W^T (Eq. (10) with S = diag(w)), built densely."""
+    rng = np.random.default_rng(sum(grid) + 100)
+    n = 30
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    pos[2][0] = np.float32(grid[2]) - np.float32(1e-5)  # wraps in z
+    w = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    zero = [np.zeros(n, np.float32)] * 3
+    M, ninv = oracle.mass_matrix_scalar(grid, pos, w)
+    assert ninv == 0
+    want = _offset_layout(_dense_mass(grid, pos, w, zero), grid)[:, :, 0, 0]
+    assert np.abs(M.reshape(-1, 27) - want).max() <= 1e-12 * np.abs(want).max()
+    # and the tensor matrix with omega = 0 (alpha = I) carries it on its diagonal
+    Mt, _ = oracle.mass_matrix(grid, pos, w, zero)
+    for i in range(3):
+        assert np.abs(Mt[..., i, i] - M).max() <= 1e-12 * np.abs(M).max()
+
+
+def test_scalar_mass_matrix_row_sums_and_symmetry():
+    """sum_o M[g][o] = sum_p w W_pg (partition of unity), and M[g][o] = M[g+d][-o]."""
+    grid = (6, 5, 4)
+    rng = np.random.default_rng(7)
+    n = 400
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    w = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    M, _ = oracle.mass_matrix_scalar(grid, pos, w)
+    ones, zeros = np.ones(n, np.float32), np.zeros(n, np.float32)
+    rho = oracle.deposit_current(grid, 1, pos, [ones, zeros, zeros], w)[0][0]
+    assert np.abs(M.sum(axis=-1) - rho).max() <= 1e-12 * np.abs(rho).max()
+    for o in range(27):
+        dz, dy, dx = o // 9 - 1, (o // 3) % 3 - 1, o % 3 - 1
+        mirrored = np.roll(M[..., 26 - o], shift=(-dz, -dy, -dx), axis=(0, 1, 2))
+        assert np.abs(M[..., o] - mirrored).max() <= 1e-12 * np.abs(M).max()
+
+
 def test_mass_matrix_invariants():
     grid = (6, 5, 4)
     Nx, Ny, Nz = grid
