@@ -64,23 +64,41 @@ def load_traffic():
     out = {}
     if not os.path.exists(p):
         return out
-    cur = source_hash()
     with open(p) as f:
         for line in f:
             line = line.split("#", 1)[0].split()
-            if len(line) == 4 and line[3] == cur:
+            if len(line) == 4 and line[3] == source_hash(line[0]):
                 out[line[0]] = (float(line[1]), float(line[2]))
     return out
 
 
-def source_hash():
+# The source files each timed kernel is built from (all of them for a name not listed).
+_COMMON = ["common.cuh", "profile.cuh"]
+KERNEL_SOURCES = {
+    "sort": ["tile_sort.cu"] + _COMMON,
+    "deposit_tiled": ["deposit_tiled.cuh", "deposit.cuh", "deposit_2d.cu", "deposit_3d.cu"] + _COMMON,
+    "deposit_zigzag": ["deposit_zigzag.cu", "deposit_tiled.cuh", "deposit.cuh"] + _COMMON,
+    "mass": ["mass_matrix.cu", "tcgen05.cuh"] + _COMMON,
+    "cic1d": ["cic1d.cu"] + _COMMON,
+}
+
+
+def source_hash(kernel=None):
+    """Hash of the sources a kernel is built from (prefix match on its timer name)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "particle_cell_grid_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+    files = None
+    if kernel is not None:
+        for key, fl in KERNEL_SOURCES.items():
+            if kernel.startswith(key):
+                files = fl
+                break
+    if files is None:
+        files = [fn for fn in os.listdir(csrc) if fn.endswith((".cu", ".cuh"))]
+    for fn in sorted(files):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:12]
 
 
@@ -416,7 +434,20 @@ def mass_workload(pcg, steps, warmup, dist, peaks, traffic, edge=64):
             r["tensor_frac_issued"] = round(issued[prec] / (kms * 1e-3) / 1e12 / pk, 4)
             r["tensor_peak_tflops"] = pk
         res[prec] = r
-    del dp, out, offs, M
+    # the scalar (MPM) matrix of the same particles: one component, 27 floats per node
+    Ms = torch.empty(tuple(reversed(grid)) + (27,), dtype=torch.float32, device="cuda")
+    alg_s = n * 16 + Ms.numel() * 4
+    sc = {"workload": f"scalar mass matrix, same particles ({edge}^3 x 64 ppc, 27 offsets)"}
+    for prec in ("tf32", "bf16", "simt"):
+        step = lambda: pcg.assemble_mass_matrix_scalar(grid, out[:3], out[3], offs, precision=prec, M=Ms)
+        step()
+        ms = time_steps(step, steps, warmup, dist, stream, pcg=pcg)
+        timed = pcg.profile_collect()
+        ent = roofline_entry(f"mass_scalar_{prec}", timed, alg_s, peaks["hbm_gbs"], traffic, n)
+        sc[prec] = {"ms_per_call": round(ms / steps, 4), "kernel_ms": ent["avg_ms"],
+                    "M_particles_per_s": round(n / (ms / steps * 1e-3) / 1e6, 1), "roofline": ent}
+    res["scalar"] = sc
+    del dp, out, offs, M, Ms
     torch.cuda.empty_cache()
     return res
 

@@ -333,6 +333,26 @@ PCG_API pcg_status pcg_assemble_mass_matrix(const int32_t *grid, int32_t order, 
                                     size_t workspace_bytes, void *stream);
 
 /* -------------------------------------------------------------------------
+ * Scalar mass matrix with first-order (CIC) B-splines.
+ * Defined by Pennati & Markidis, Sec. 2.1 after Eq. (6): the scalar case
+ * s_p^{ij} = q_p delta^{ij} (e.g. the MPM mass matrix), one component per node
+ * pair:  M_{g g'} = sum_p w_p W_pg W_pg'  (sigma = 1), assembled and stored as
+ * for pcg_assemble_mass_matrix (Sec. 3.1-3.4) with NC = 1.
+ *
+ * Output layout: M[g][o], o as above; float[ncells][27].
+ *   grid, order, precision, n, pos, cell_offsets, stats: as for
+ *              pcg_assemble_mass_matrix (precision 0 = TF32 and 1 = BF16 tensor
+ *              cores, 2 = fp32 CUDA cores).
+ *   w          device float[n] (the per-particle coefficient, e.g. the mass).
+ *   M          device float[ncells * 27], 16-byte aligned, output (overwritten).
+ * Launches: 2 (zero M + assembly).  No workspace.
+ */
+PCG_API pcg_status pcg_assemble_mass_matrix_scalar(const int32_t *grid, int32_t order, int32_t precision,
+                                                   int64_t n, const float *const *pos, const float *w,
+                                                   const uint32_t *cell_offsets, float *M,
+                                                   pcg_stats *stats, void *stream);
+
+/* -------------------------------------------------------------------------
  * Kernel timing (tracing aid; no counterpart in the method).
  * While enabled, every kernel the library launches is bracketed by two CUDA
  * events recorded on its launch stream.  pcg_profile_collect() waits for the

@@ -8,7 +8,7 @@ allocated with torch; workspaces likewise.
 
 Entry points (same names as the C ABI without the ``pcg_`` prefix):
   deposit_cic1d, deposit_cic1d_grad, tile_sort, deposit_current, deposit_zigzag,
-  assemble_mass_matrix,
+  assemble_mass_matrix, assemble_mass_matrix_scalar,
   plus the *_workspace_size queries and stats helpers.
 """
 from __future__ import annotations
@@ -23,6 +23,7 @@ from ._lib import PcgError, check
 __all__ = [
     "PcgError", "version", "deposit_cic1d", "deposit_cic1d_grad", "tile_sort", "tile_sort_workspace_size",
     "deposit_current", "deposit_current_workspace_size", "deposit_zigzag", "assemble_mass_matrix",
+    "assemble_mass_matrix_scalar",
     "assemble_mass_matrix_workspace_size", "new_stats", "read_stats", "n_tiles",
     "profile_enable", "profile_collect",
 ]
@@ -260,6 +261,23 @@ def assemble_mass_matrix(grid, pos, w, omega, cell_offsets, precision="tf32", M=
                                               _ptr_arr(omega, 3), _ptr(cell_offsets), _ptr(M), _ptr(stats),
                                               _ptr(ws), _ws_bytes(ws), _stream(stream))
     check(st, "pcg_assemble_mass_matrix")
+    return M
+
+
+def assemble_mass_matrix_scalar(grid, pos, w, cell_offsets, precision="tf32", M=None, stats=None, stream=None):
+    """Scalar mass matrix M[g][o] (float32[Nz, Ny, Nx, 27]) = sum_p w W_pg W_pg' from
+    cell-sorted particles."""
+    n = w.numel()
+    for i, t in enumerate(pos):
+        _dev(t, torch.float32, f"pos[{i}]")
+    _dev(w, torch.float32, "w")
+    _dev(cell_offsets, None, "cell_offsets")
+    shape = tuple(int(N) for N in reversed(grid)) + (27,)
+    M = torch.empty(shape, dtype=torch.float32, device=w.device) if M is None else _dev(M, torch.float32, "M")
+    st = _lib.load().pcg_assemble_mass_matrix_scalar(_grid_arr(grid), 1, PRECISION[precision], n, _ptr_arr(pos, 3),
+                                                     _ptr(w), _ptr(cell_offsets), _ptr(M), _ptr(stats),
+                                                     _stream(stream))
+    check(st, "pcg_assemble_mass_matrix_scalar")
     return M
 
 

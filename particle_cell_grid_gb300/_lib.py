@@ -40,6 +40,7 @@ SIGNATURES = {
     "pcg_profile_enable": (ctypes.c_int, [_i32]),
     "pcg_profile_collect": (ctypes.c_int, [_i32, _vp, _vp, _vp, _P(_i32)]),
     "pcg_assemble_mass_matrix_workspace_size": (ctypes.c_int, [_vp, _i64, _P(_sz)]),
+    "pcg_assemble_mass_matrix_scalar": (ctypes.c_int, [_vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "pcg_assemble_mass_matrix": (ctypes.c_int, [_vp, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp,
                                                 _vp, _sz, _vp]),
 }

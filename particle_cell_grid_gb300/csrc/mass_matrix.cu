@@ -47,38 +47,44 @@ constexpr int KB = 64;             // particles per batch: the K extent of one c
 constexpr int G = 4;               // batches (cell products) per iteration
 constexpr int BC = 4;              // cell-block edge
 constexpr int WN = BC + 1;         // node-window edge
-// A window row of 5 node blocks (1215 floats) starts 0-3 floats into its 1220-float
+// Node blocks: 27 offsets x NC components (NC = 9 for the ECSIM tensor, 1 for
+// the scalar matrix).  A window row of 5 node blocks starts 0-3 floats into its
 // slot, so that it has the same alignment modulo 16 bytes as its place in M.
-constexpr int ACC_ROW = 1220;
-constexpr int ACC_FLOATS = WN * WN * ACC_ROW;
-constexpr int ACC_BYTES = (ACC_FLOATS * 4 + 1023) / 1024 * 1024;
+template <int NC>
+struct Win {
+    static constexpr int NB = 27 * NC;                                   // floats per node block
+    static constexpr int ACC_ROW = (WN * NB + 3 + 3) / 4 * 4;            // 1220 (NC 9), 140 (NC 1)
+    static constexpr int ACC_FLOATS = WN * WN * ACC_ROW;
+    static constexpr int ACC_BYTES = (ACC_FLOATS * 4 + 1023) / 1024 * 1024;
+};
 constexpr uint32_t kTmemCols = 64;  // G accumulators of 16 columns
 constexpr uint32_t kMaxPolls = 1u << 22;
 
 enum Mode { TF32 = 0, BF16 = 1, SIMT = 2 };
 
-// Staging of one batch (128-byte swizzle, K-major):
-//   TF32: K = 64 x 4 B = 256 B per row = two 128-byte K-atoms; per K-atom the 72
-//         A rows are 9 atoms of 8 rows (9 KB), B's 8 rows one atom (1 KB).
-//         [A k0 | A k1 | B k0 | B k1] = 20 KB.
-//   BF16: K = 64 x 2 B = one K-atom.  [A | B] = 10 KB.
-template <int MODE>
+// Staging of one batch (128-byte swizzle, K-major), NC components:
+//   TF32: K = 64 x 4 B = 256 B per row = two 128-byte K-atoms; per K-atom the
+//         8 NC A rows are NC atoms of 8 rows, B's 8 rows one atom (1 KB).
+//         [A k0 | A k1 | B k0 | B k1] = 20 KB for NC = 9, 4 KB for NC = 1.
+//   BF16: K = 64 x 2 B = one K-atom.  [A | B].
+template <int MODE, int NC>
 struct Op {
     static constexpr int KATOMS = MODE == TF32 ? 2 : 1;
-    static constexpr int A_KSTRIDE = 9 * 1024;               // A bytes per K-atom
+    static constexpr int A_KSTRIDE = NC * 1024;              // A bytes per K-atom
     static constexpr int A_BYTES = KATOMS * A_KSTRIDE;
     static constexpr int B_BYTES = KATOMS * 1024;
     static constexpr int BATCH = A_BYTES + B_BYTES;
     // the MMA reads 16 row atoms of A and 2 of B from each K-atom base: the last
-    // batch's reads run up to 7 KB past its A and 1 KB past its B
-    static constexpr int STAGING = G * BATCH + 8 * 1024;
+    // batch's reads run up to 16 - NC KB past its A and 1 KB past its B (they
+    // land in the node window that follows and are never read back)
+    static constexpr int STAGING = G * BATCH + (17 - NC) * 1024;
     static constexpr int KSTEPS = MODE == TF32 ? KB / 8 : KB / 16;
     static constexpr int EB = MODE == TF32 ? 4 : 2;           // element bytes
 };
 
-template <>
-struct Op<SIMT> {
-    static constexpr int STAGING = G * KB * 17 * 4;  // per particle: W[8], s[9]
+template <int NC>
+struct Op<SIMT, NC> {
+    static constexpr int STAGING = G * KB * (8 + NC) * 4;  // per particle: W[8], s[NC]
 };
 
 struct Args {
@@ -111,20 +117,28 @@ __device__ __forceinline__ void alpha_w(float w, float ox, float oy, float oz, f
     s[8] = f * (1.f + oz * oz);
 }
 
+// Per-particle coefficients: w alpha (NC = 9) or w (NC = 1, the scalar case of Eq. (6)).
+template <int NC>
+__device__ __forceinline__ void coeffs(float w, float ox, float oy, float oz, float (&s)[NC]) {
+    if constexpr (NC == 9) alpha_w(w, ox, oy, oz, s);
+    else s[0] = w;
+}
+
 __device__ __forceinline__ float corner_w(int a, float fx, float fy, float fz) {
     return ((a & 1) ? fx : 1.f - fx) * ((a & 2) ? fy : 1.f - fy) * ((a & 4) ? fz : 1.f - fz);
 }
 
 __device__ __forceinline__ int wrapi(int i, int N) { return i >= N ? i - N : (i < 0 ? i + N : i); }
 
-// Slow path for a particle not inside the cell it is listed under: all 8x8x9
+// Slow path for a particle not inside the cell it is listed under: all 8x8xNC
 // contributions straight to global M.
+template <int NC>
 __device__ void particle_global(const Args &A, float x, float y, float z, float w, float ox,
                                 float oy, float oz) {
     const int ix = (int)x, iy = (int)y, iz = (int)z;
     const float fx = x - ix, fy = y - iy, fz = z - iz;
-    float s[9];
-    alpha_w(w, ox, oy, oz, s);
+    float s[NC];
+    coeffs<NC>(w, ox, oy, oz, s);
     for (int a = 0; a < 8; ++a) {
         const int gx = wrapi(ix + (a & 1), A.N[0]);
         const int gy = wrapi(iy + ((a >> 1) & 1), A.N[1]);
@@ -135,7 +149,7 @@ __device__ void particle_global(const Args &A, float x, float y, float z, float 
             const int o = (((b >> 2) - (a >> 2)) + 1) * 9 + ((((b >> 1) & 1) - ((a >> 1) & 1)) + 1) * 3 +
                           ((b & 1) - (a & 1)) + 1;
             const float WW = Wa * corner_w(b, fx, fy, fz);
-            for (int c = 0; c < 9; ++c) red_add_f32(A.M + (g * 27 + o) * 9 + c, s[c] * WW);
+            for (int c = 0; c < NC; ++c) red_add_f32(A.M + (g * 27 + o) * NC + c, s[c] * WW);
         }
     }
 }
@@ -146,6 +160,7 @@ struct Raw {
     bool live;
 };
 
+template <int NC>
 __device__ __forceinline__ Raw load_raw(const Args &A, const Batch &b, int k) {
     Raw r;
     r.live = b.ci >= 0 && k < (int)b.len;
@@ -155,9 +170,13 @@ __device__ __forceinline__ Raw load_raw(const Args &A, const Batch &b, int k) {
         r.y = A.y[p];
         r.z = A.z[p];
         r.w = A.w[p];
-        r.ox = A.ox[p];
-        r.oy = A.oy[p];
-        r.oz = A.oz[p];
+        if (NC == 9) {
+            r.ox = A.ox[p];
+            r.oy = A.oy[p];
+            r.oz = A.oz[p];
+        } else {
+            r.ox = r.oy = r.oz = 0.f;
+        }
     } else {
         r.x = r.y = r.z = r.w = r.ox = r.oy = r.oz = 0.f;
     }
@@ -167,8 +186,9 @@ __device__ __forceinline__ Raw load_raw(const Args &A, const Batch &b, int k) {
 // Weights and coefficients of a loaded particle for the cell (cx, cy, cz); a
 // particle outside that cell is flagged, deposited by the slow path and
 // contributes zeros here.
+template <int NC>
 __device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int cy, int cz,
-                                        bool owner, float (&W)[8], float (&s)[9]) {
+                                        bool owner, float (&W)[8], float (&s)[NC]) {
     bool use = r.live;
     if (use) {
         const bool inside = r.x >= (float)cx && r.x < (float)(cx + 1) && r.y >= (float)cy &&
@@ -177,7 +197,7 @@ __device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int
             const bool ok = r.x >= 0.f && r.x < (float)A.N[0] && r.y >= 0.f && r.y < (float)A.N[1] &&
                             r.z >= 0.f && r.z < (float)A.N[2];
             if (owner) {  // once per particle, by one of the threads sharing it
-                if (ok) particle_global(A, r.x, r.y, r.z, r.w, r.ox, r.oy, r.oz);
+                if (ok) particle_global<NC>(A, r.x, r.y, r.z, r.w, r.ox, r.oy, r.oz);
                 if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
             }
             use = false;
@@ -187,7 +207,7 @@ __device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int
 #pragma unroll
         for (int a = 0; a < 8; ++a) W[a] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 9; ++c) s[c] = 0.f;
+        for (int c = 0; c < NC; ++c) s[c] = 0.f;
         return false;
     }
     const float fx = r.x - (float)cx, fy = r.y - (float)cy, fz = r.z - (float)cz;
@@ -201,7 +221,7 @@ __device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int
     W[5] = fx * yz01;
     W[6] = gx * yz11;
     W[7] = fx * yz11;
-    alpha_w(r.w, r.ox, r.oy, r.oz, s);
+    coeffs<NC>(r.w, r.ox, r.oy, r.oz, s);
     return true;
 }
 
@@ -227,12 +247,14 @@ __device__ __forceinline__ bool next_batches(const unsigned *cstart, const unsig
     return any;
 }
 
-template <int MODE>
+template <int MODE, int NC>
 __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
+    using Wn = Win<NC>;
+    constexpr int NB = Wn::NB, ACC_ROW = Wn::ACC_ROW, ACC_FLOATS = Wn::ACC_FLOATS;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *stage = smem;  // 1024-aligned operand staging first
-    float *acc = reinterpret_cast<float *>(smem + Op<MODE>::STAGING);
-    unsigned *cstart = reinterpret_cast<unsigned *>(smem + Op<MODE>::STAGING + ACC_BYTES);
+    float *acc = reinterpret_cast<float *>(smem + Op<MODE, NC>::STAGING);
+    unsigned *cstart = reinterpret_cast<unsigned *>(smem + Op<MODE, NC>::STAGING + Wn::ACC_BYTES);
     unsigned *ccount = cstart + 64;
     int *rsh = reinterpret_cast<int *>(ccount + 64);  // window row shifts (floats)
     uint64_t *mbar = reinterpret_cast<uint64_t *>(rsh + 32);
@@ -279,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
             const int row = tid - 64;
             const int gy = (by * BC + row % WN) % A.N[1], gz = (bz * BC + row / WN) % A.N[2];
             const long long node = ((long long)gz * A.N[1] + gy) * A.N[0] + (bx * BC) % A.N[0];
-            rsh[row] = (int)((node * 243) & 3);
+            rsh[row] = (int)((node * NB) & 3);
         }
         __syncthreads();
 
@@ -287,20 +309,20 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
         unsigned cur_k = 0;
         Batch bt[G];
         bool any = next_batches(cstart, ccount, cur, cur_k, bt);
-        Raw raw = load_raw(A, bt[jme], kme);
+        Raw raw = load_raw<NC>(A, bt[jme], kme);
         while (any) {
             const Batch mine = bt[jme];
             const int cx = bx * BC + (mine.ci & 3), cy = by * BC + ((mine.ci >> 2) & 3),
                       cz = bz * BC + (mine.ci >> 4);
-            float W[8], s[9];
-            prepare(A, raw, cx, cy, cz, half == 0, W, s);
+            float W[8], s[NC];
+            prepare<NC>(A, raw, cx, cy, cz, half == 0, W, s);
 
             float d[2][8];   // this thread's rows of up to two batches
             int dj[2] = {-1, -1};
             Batch nbt[G];
             bool nany;
             if constexpr (MODE != SIMT) {
-                using O = Op<MODE>;
+                using O = Op<MODE, NC>;
                 // ---- this particle's column of A = [W S^ij] and B = W^T (128-byte swizzle) ----
                 {
                     unsigned char *Aj = stage + jme * O::BATCH;
@@ -314,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                     for (int a = 0; a < 8; ++a) {
                         const int off = a * 128 + ((chunk ^ a) << 4);
 #pragma unroll
-                        for (int c = 0; c < 9; ++c) {
-                            if ((c < 5) != (half == 0)) continue;
+                        for (int c = 0; c < NC; ++c) {
+                            // components split between the particle's two threads
+                            if ((c < (NC + 1) / 2) != (half == 0)) continue;
                             const float v = s[c] * W[a];
                             unsigned char *dst = abase + c * 1024 + off;
                             if (MODE == TF32) *reinterpret_cast<uint32_t *>(dst) = tc::to_tf32(v);
@@ -359,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                 }
                 // the next group's particles load while the tensor core works
                 nany = next_batches(cstart, ccount, cur, cur_k, nbt);
-                raw = load_raw(A, nbt[jme], kme);
+                raw = load_raw<NC>(A, nbt[jme], kme);
 
                 const bool late = __syncthreads_or(!tc::mbar_wait(mbar, phase, kMaxPolls));
                 if (late) {
@@ -373,40 +396,41 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                 // ---- read the accumulators back: warp quadrant q holds rows 32q..32q+31 ----
                 const int q = warp & 3;
                 const int jj = warp >> 2;  // one batch per warp: warps 4j..4j+3 cover its 128 lanes
-                if (q < 3 && bt[jj].ci >= 0) {  // warp-uniform
+                if (32 * q < 8 * NC && bt[jj].ci >= 0) {  // warp-uniform
                     tc::tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + 16 * jj, d[0]);
                     dj[0] = jj;
                 }
                 tc::fence_before_sync();
             } else {
                 // ---- CUDA-core baseline: per-particle W and s staged in shared memory ----
-                float *ps = reinterpret_cast<float *>(stage);  // [G][KB][17]
+                constexpr int PS = 8 + NC;                      // floats per particle
+                float *ps = reinterpret_cast<float *>(stage);  // [G][KB][PS]
                 if (half == 0) {
-                    float *dst = ps + (size_t)pme * 17;
+                    float *dst = ps + (size_t)pme * PS;
 #pragma unroll
                     for (int a = 0; a < 8; ++a) dst[a] = W[a];
 #pragma unroll
-                    for (int c = 0; c < 9; ++c) dst[8 + c] = s[c];
+                    for (int c = 0; c < NC; ++c) dst[8 + c] = s[c];
                 }
                 nany = next_batches(cstart, ccount, cur, cur_k, nbt);
-                raw = load_raw(A, nbt[jme], kme);
+                raw = load_raw<NC>(A, nbt[jme], kme);
                 __syncthreads();
                 const int q = warp & 3;
                 const int r = 32 * q + lane;
 #pragma unroll
                 for (int h = 0; h < 1; ++h) {
                     const int jj = warp >> 2;
-                    if (q >= 3 || bt[jj].ci < 0) continue;
+                    if (32 * q >= 8 * NC || bt[jj].ci < 0) continue;
                     dj[h] = jj;
 #pragma unroll
                     for (int nn = 0; nn < 8; ++nn) d[h][nn] = 0.f;
-                    if (r < 72) {
+                    if (r < 8 * NC) {
                         const int c = r >> 3, a = r & 7;
-                        const float *pj = ps + (size_t)jj * KB * 17;
+                        const float *pj = ps + (size_t)jj * KB * PS;
                         for (int k = 0; k < KB; ++k) {
-                            const float f = pj[k * 17 + 8 + c] * pj[k * 17 + a];
+                            const float f = pj[k * PS + 8 + c] * pj[k * PS + a];
 #pragma unroll
-                            for (int nn = 0; nn < 8; ++nn) d[h][nn] = fmaf(f, pj[k * 17 + nn], d[h][nn]);
+                            for (int nn = 0; nn < 8; ++nn) d[h][nn] = fmaf(f, pj[k * PS + nn], d[h][nn]);
                         }
                     }
                 }
@@ -415,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
             // ---- epilogue: add the 8x8 block rows into the node window ----
             {
                 const int r = 32 * (warp & 3) + lane;
-                if (r < 72) {
+                if (r < 8 * NC) {
                     const int c = r >> 3, a = r & 7;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -424,13 +448,13 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                         const int nx = (ci & 3) + (a & 1), ny = ((ci >> 2) & 3) + ((a >> 1) & 1),
                                   nz = (ci >> 4) + (a >> 2);
                         const int wr = nz * WN + ny;
-                        float *row = acc + wr * ACC_ROW + rsh[wr] + nx * 243 + c;
+                        float *row = acc + wr * ACC_ROW + rsh[wr] + nx * NB + c;
 #pragma unroll
                         for (int nn = 0; nn < 8; ++nn) {
                             const int o = ((nn >> 2) - (a >> 2) + 1) * 9 +
                                           (((nn >> 1) & 1) - ((a >> 1) & 1) + 1) * 3 +
                                           ((nn & 1) - (a & 1) + 1);
-                            red_shared_add_f32(row + o * 9, d[h][nn]);
+                            red_shared_add_f32(row + o * NC, d[h][nn]);
                         }
                     }
                 }
@@ -454,9 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                 const int gx0 = (bx * BC + nx0) % A.N[0];
                 int len = WN - nx0;
                 if (gx0 + len > A.N[0]) len = A.N[0] - gx0;  // the row wraps at the x boundary
-                float *dst = A.M + (((long long)gz * A.N[1] + gy) * A.N[0] + gx0) * 243;
-                const float *sp = src + nx0 * 243;
-                const int L = len * 243;
+                float *dst = A.M + (((long long)gz * A.N[1] + gy) * A.N[0] + gx0) * NB;
+                const float *sp = src + nx0 * NB;
+                const int L = len * NB;
                 const int head = min((int)((16 - (reinterpret_cast<uintptr_t>(dst) & 15)) & 15) / 4, L);
                 const bool same = ((reinterpret_cast<uintptr_t>(sp + head) & 15) == 0) &&
                                   ((reinterpret_cast<uintptr_t>(dst + head) & 15) == 0);
@@ -498,20 +522,23 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
     }
 }
 
-template <int MODE>
+template <int MODE, int NC>
 size_t smem_bytes() {
-    return Op<MODE>::STAGING + ACC_BYTES + 64 * 8 + 32 * 4 + 16;
+    return Op<MODE, NC>::STAGING + Win<NC>::ACC_BYTES + 64 * 8 + 32 * 4 + 16;
 }
 
-template <int MODE>
+template <int MODE, int NC>
 pcg_status launch(const Args &A, cudaStream_t s) {
-    const size_t smem = smem_bytes<MODE>();
-    PCG_CHECK_CUDA(cudaFuncSetAttribute(mass_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = smem_bytes<MODE, NC>();
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(mass_kernel<MODE, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)smem));
     const long long nblocks = (long long)A.nb[0] * A.nb[1] * A.nb[2];
     const long long grid = nblocks < num_sms() ? nblocks : num_sms();
-    prof::Mark mk(MODE == TF32 ? "mass_matrix_tf32" : MODE == BF16 ? "mass_matrix_bf16" : "mass_matrix_simt", s);
-    mass_kernel<MODE><<<(unsigned)grid, kThreads, smem, s>>>(A);
+    static const char *const names[2][3] = {
+        {"mass_matrix_tf32", "mass_matrix_bf16", "mass_matrix_simt"},
+        {"mass_scalar_tf32", "mass_scalar_bf16", "mass_scalar_simt"}};
+    prof::Mark mk(names[NC == 1][MODE], s);
+    mass_kernel<MODE, NC><<<(unsigned)grid, kThreads, smem, s>>>(A);
     return launch_status();
 }
 
@@ -525,16 +552,15 @@ extern "C" pcg_status pcg_assemble_mass_matrix_workspace_size(const int32_t *gri
     return PCG_OK;
 }
 
-extern "C" pcg_status pcg_assemble_mass_matrix(const int32_t *grid, int32_t order,
-                                               int32_t precision, int64_t n,
-                                               const float *const *pos, const float *w,
-                                               const float *const *omega,
-                                               const uint32_t *cell_offsets, float *M,
-                                               pcg_stats *stats, void *workspace,
-                                               size_t workspace_bytes, void *stream) {
-    using namespace pcg;
-    (void)workspace;
-    (void)workspace_bytes;
+namespace pcg {
+namespace mm {
+namespace {
+
+// Shared body of the tensor (NC = 9) and scalar (NC = 1) entry points.
+template <int NC>
+pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64_t n, const float *const *pos,
+                    const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
+                    pcg_stats *stats, void *stream) {
     if (grid == nullptr || order != 1 || n < 0 || n >= 0xffffffffll) return PCG_ERR_INVALID_ARG;
     if (precision < 0 || precision > 2) return PCG_ERR_INVALID_ARG;
     long long ncells = 1;
@@ -544,14 +570,15 @@ extern "C" pcg_status pcg_assemble_mass_matrix(const int32_t *grid, int32_t orde
     }
     if (ncells >= (1ll << 31)) return PCG_ERR_INVALID_ARG;
     if (M == nullptr || !aligned16(M) || cell_offsets == nullptr) return PCG_ERR_INVALID_ARG;
-    if (n > 0 && (pos == nullptr || omega == nullptr || w == nullptr || pos[0] == nullptr ||
-                  pos[1] == nullptr || pos[2] == nullptr || omega[0] == nullptr ||
-                  omega[1] == nullptr || omega[2] == nullptr))
+    if (n > 0 && (pos == nullptr || w == nullptr || pos[0] == nullptr || pos[1] == nullptr || pos[2] == nullptr))
         return PCG_ERR_INVALID_ARG;
-    mm::Args A{};
+    if (NC == 9 && n > 0 &&
+        (omega == nullptr || omega[0] == nullptr || omega[1] == nullptr || omega[2] == nullptr))
+        return PCG_ERR_INVALID_ARG;
+    Args A{};
     for (int mu = 0; mu < 3; ++mu) {
         A.N[mu] = grid[mu];
-        A.nb[mu] = (grid[mu] + mm::BC - 1) / mm::BC;
+        A.nb[mu] = (grid[mu] + BC - 1) / BC;
     }
     A.ncells = ncells;
     if (n > 0) {
@@ -559,20 +586,45 @@ extern "C" pcg_status pcg_assemble_mass_matrix(const int32_t *grid, int32_t orde
         A.y = pos[1];
         A.z = pos[2];
         A.w = w;
-        A.ox = omega[0];
-        A.oy = omega[1];
-        A.oz = omega[2];
+        if (NC == 9) {
+            A.ox = omega[0];
+            A.oy = omega[1];
+            A.oz = omega[2];
+        }
     }
     A.offs = cell_offsets;
     A.n = n;
     A.M = M;
     A.flags = stats ? &stats->error_flags : nullptr;
     cudaStream_t s = as_stream(stream);
-    pcg_status st = zero_f32(M, (size_t)ncells * 243, s);
+    pcg_status st = zero_f32(M, (size_t)ncells * Win<NC>::NB, s);
     if (st != PCG_OK || n == 0) return st;
     switch (precision) {
-        case 0: return mm::launch<mm::TF32>(A, s);
-        case 1: return mm::launch<mm::BF16>(A, s);
-        default: return mm::launch<mm::SIMT>(A, s);
+        case 0: return launch<TF32, NC>(A, s);
+        case 1: return launch<BF16, NC>(A, s);
+        default: return launch<SIMT, NC>(A, s);
     }
+}
+
+}  // namespace
+}  // namespace mm
+}  // namespace pcg
+
+extern "C" pcg_status pcg_assemble_mass_matrix(const int32_t *grid, int32_t order,
+                                               int32_t precision, int64_t n,
+                                               const float *const *pos, const float *w,
+                                               const float *const *omega,
+                                               const uint32_t *cell_offsets, float *M,
+                                               pcg_stats *stats, void *workspace,
+                                               size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    return pcg::mm::assemble<9>(grid, order, precision, n, pos, w, omega, cell_offsets, M, stats, stream);
+}
+
+extern "C" pcg_status pcg_assemble_mass_matrix_scalar(const int32_t *grid, int32_t order, int32_t precision,
+                                                      int64_t n, const float *const *pos, const float *w,
+                                                      const uint32_t *cell_offsets, float *M, pcg_stats *stats,
+                                                      void *stream) {
+    return pcg::mm::assemble<1>(grid, order, precision, n, pos, w, nullptr, cell_offsets, M, stats, stream);
 }

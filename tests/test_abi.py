@@ -153,3 +153,16 @@ def test_mass_matrix_rejects_bad_arguments(lib):
     assert call(order=2) == 1
     assert call(prec=3) == 1
     assert call(M=ctypes.c_void_p(260)) == 1
+
+
+def test_scalar_mass_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p(4096)
+    arr = (ctypes.c_void_p * 3)(4096, 4096, 4096)
+    f = lib.pcg_assemble_mass_matrix_scalar
+    g = _grid(8, 8, 8)
+    assert f(g, 2, 0, 10, arr, vp, vp, vp, None, None) == 1           # order 2
+    assert f(g, 1, 3, 10, arr, vp, vp, vp, None, None) == 1           # precision
+    assert f(_grid(8, 2, 8), 1, 0, 10, arr, vp, vp, vp, None, None) == 1
+    assert f(g, 1, 0, 10, None, vp, vp, vp, None, None) == 1          # no positions
+    assert f(g, 1, 0, 10, arr, vp, None, vp, None, None) == 1         # no cell offsets
+    assert f(g, 1, 0, 10, arr, vp, vp, ctypes.c_void_p(4100), None, None) == 1  # M unaligned

@@ -81,3 +81,53 @@ def test_empty():
     offs = np.zeros(65, np.int32)
     M = pcg.assemble_mass_matrix(grid, [dev(z)] * 3, dev(z), [dev(z)] * 3, dev(offs))
     assert np.all(host(M) == 0)
+
+
+# ---------------------------------------------------------------------------
+# scalar (MPM) mass matrix: the same assembly with one component
+def _assemble_scalar(pcg, grid, pos, w, precision):
+    dp = [dev(p) for p in pos]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(w)])
+    stats = pcg.new_stats()
+    M = pcg.assemble_mass_matrix_scalar(grid, out[:3], out[3], offs, precision=precision, stats=stats)
+    return host(M), stats_dict(stats)
+
+
+@pytest.mark.parametrize("precision", ["tf32", "bf16", "simt"])
+@pytest.mark.parametrize("grid,ppc", [((16, 16, 16), 64), ((5, 4, 6), 100), ((3, 3, 3), 7)])
+def test_scalar_matches_oracle(precision, grid, ppc):
+    pcg = need_gpu()
+    d = synth.mass3d(grid=grid, ppc=ppc, seed=sum(grid) + ppc)
+    M, st = _assemble_scalar(pcg, grid, d["pos"], d["w"], precision)
+    Mr, _ = oracle.mass_matrix_scalar(grid, d["pos"], d["w"])
+    assert M.shape == Mr.shape
+    assert rel_frobenius(M, Mr) <= TOL[precision]
+    assert st["error_flags"] == 0
+
+
+@pytest.mark.parametrize("precision", ["tf32", "simt"])
+def test_scalar_variable_occupancy_and_mismatch(precision):
+    pcg = need_gpu()
+    grid = (9, 7, 8)
+    rng = np.random.default_rng(11)
+    ncell = int(np.prod(grid))
+    counts = rng.integers(0, 200, ncell)
+    counts[::5] = 0
+    cell = np.repeat(np.arange(ncell), counts)
+    n = cell.size
+    coords = [cell % grid[0], (cell // grid[0]) % grid[1], cell // (grid[0] * grid[1])]
+    pos = [synth._inside_cell_f32(c, rng.random(n))[rng.permutation(n)] for c in coords]
+    w = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    M, st = _assemble_scalar(pcg, grid, pos, w, precision)
+    Mr, _ = oracle.mass_matrix_scalar(grid, pos, w)
+    assert rel_frobenius(M, Mr) <= TOL[precision]
+    # arrays that no longer match their cell layout: exact through the slow path, flagged
+    dp = [dev(p) for p in pos]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(w)])
+    perm = np.random.default_rng(2).permutation(n)
+    arrs = [host(t)[perm] for t in out]
+    stats = pcg.new_stats()
+    M = pcg.assemble_mass_matrix_scalar(grid, [dev(a) for a in arrs[:3]], dev(arrs[3]), offs,
+                                        precision=precision, stats=stats)
+    assert rel_frobenius(host(M), Mr) <= TOL[precision]
+    assert stats_dict(stats)["error_flags"] & 2
