@@ -27,11 +27,16 @@
 //    the particle's corner weights and coefficients stay in registers.
 //  * The next batch group's particles are loaded into registers while the
 //    tensor core runs on the current one.
-//  * A CTA walks 4x4x4-cell blocks; each block's 5x5x5 node window of
-//    243-float blocks (121.5 KB) is accumulated in shared memory and flushed
-//    once to global M, ~1.95 node blocks of reductions per cell instead of 8:
-//    each window row (5 nodes, contiguous in M) goes out as one asynchronous
-//    bulk reduce-add on the TMA engine, issued by one thread.
+//  * A CTA of 256 threads walks 4x4x2-cell blocks; each block's 5x5x3 node
+//    window of 243-float blocks (71 KB) is accumulated in shared memory and
+//    flushed once to global M, ~2.3 node blocks of reductions per cell instead
+//    of 8: each window row (5 nodes, contiguous in M) goes out as one
+//    asynchronous bulk reduce-add on the TMA engine, issued by one thread.
+//    Two CTAs share an SM (113 KB of shared memory each for TF32), so that one
+//    CTA's staging and epilogue run while the other waits on its MMAs.  One
+//    512-thread CTA per SM with 4x4x4 blocks was 1.42x slower (TF32, 64^3 x 64
+//    ppc: 2.28 vs 1.60 ms), bound by the barriers and waits of its serial
+//    stage -> MMA -> epilogue loop (37 % issue-active, 16 warps per SM).
 //  * precision 2 computes the same local products on CUDA cores (fp32 FMAs),
 //    the A/B baseline of the tensor-core kernel.
 #include <cuda_bf16.h>
@@ -42,22 +47,25 @@
 namespace pcg {
 namespace mm {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int KB = 64;             // particles per batch: the K extent of one cell product
-constexpr int G = 4;               // batches (cell products) per iteration
-constexpr int BC = 4;              // cell-block edge
-constexpr int WN = BC + 1;         // node-window edge
+constexpr int G = 2;               // batches (cell products) per iteration
+// a CTA walks blocks of BCX x BCY x BCZ cells; two CTAs share an SM
+constexpr int BCX = 4, BCY = 4, BCZ = 2;
+constexpr int NCELL = BCX * BCY * BCZ;
+constexpr int WNX = BCX + 1, WNY = BCY + 1, WNZ = BCZ + 1;  // node window
+constexpr int NROWS = WNY * WNZ;                            // window rows (x runs)
 // Node blocks: 27 offsets x NC components (NC = 9 for the ECSIM tensor, 1 for
 // the scalar matrix).  A window row of 5 node blocks starts 0-3 floats into its
 // slot, so that it has the same alignment modulo 16 bytes as its place in M.
 template <int NC>
 struct Win {
     static constexpr int NB = 27 * NC;                                   // floats per node block
-    static constexpr int ACC_ROW = (WN * NB + 3 + 3) / 4 * 4;            // 1220 (NC 9), 140 (NC 1)
-    static constexpr int ACC_FLOATS = WN * WN * ACC_ROW;
+    static constexpr int ACC_ROW = (WNX * NB + 3 + 3) / 4 * 4;           // 1220 (NC 9), 140 (NC 1)
+    static constexpr int ACC_FLOATS = NROWS * ACC_ROW;
     static constexpr int ACC_BYTES = (ACC_FLOATS * 4 + 1023) / 1024 * 1024;
 };
-constexpr uint32_t kTmemCols = 64;  // G accumulators of 16 columns
+constexpr uint32_t kTmemCols = 32;  // G accumulators of 16 columns
 constexpr uint32_t kMaxPolls = 1u << 22;
 
 enum Mode { TF32 = 0, BF16 = 1, SIMT = 2 };
@@ -74,10 +82,13 @@ struct Op {
     static constexpr int A_BYTES = KATOMS * A_KSTRIDE;
     static constexpr int B_BYTES = KATOMS * 1024;
     static constexpr int BATCH = A_BYTES + B_BYTES;
-    // the MMA reads 16 row atoms of A and 2 of B from each K-atom base: the last
-    // batch's reads run up to 16 - NC KB past its A and 1 KB past its B (they
-    // land in the node window that follows and are never read back)
-    static constexpr int STAGING = G * BATCH + (17 - NC) * 1024;
+    static constexpr int STAGING = G * BATCH;
+    // the MMA reads 16 row atoms of A and 2 of B from each K-atom base, past the
+    // last batch's own rows; those reads land in the node window that follows
+    // (never read back) and must stay inside the CTA's shared memory
+    static constexpr int READ_END_A = (G - 1) * BATCH + (KATOMS - 1) * A_KSTRIDE + 16 * 1024;
+    static constexpr int READ_END_B = (G - 1) * BATCH + A_BYTES + (KATOMS - 1) * 1024 + 2 * 1024;
+    static constexpr int READ_END = READ_END_A > READ_END_B ? READ_END_A : READ_END_B;
     static constexpr int KSTEPS = MODE == TF32 ? KB / 8 : KB / 16;
     static constexpr int EB = MODE == TF32 ? 4 : 2;           // element bytes
 };
@@ -85,6 +96,7 @@ struct Op {
 template <int NC>
 struct Op<SIMT, NC> {
     static constexpr int STAGING = G * KB * (8 + NC) * 4;  // per particle: W[8], s[NC]
+    static constexpr int READ_END = 0;
 };
 
 struct Args {
@@ -231,11 +243,11 @@ __device__ __forceinline__ bool next_batches(const unsigned *cstart, const unsig
     bool any = false;
 #pragma unroll
     for (int j = 0; j < G; ++j) {
-        while (cur < 64 && cur_k >= ccount[cur]) {
+        while (cur < NCELL && cur_k >= ccount[cur]) {
             ++cur;
             cur_k = 0;
         }
-        if (cur < 64) {
+        if (cur < NCELL) {
             const unsigned rem = ccount[cur] - cur_k;
             bt[j] = Batch{cur, cstart[cur] + cur_k, rem < (unsigned)KB ? rem : (unsigned)KB};
             cur_k += KB;
@@ -248,7 +260,7 @@ __device__ __forceinline__ bool next_batches(const unsigned *cstart, const unsig
 }
 
 template <int MODE, int NC>
-__global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
+__global__ void __launch_bounds__(kThreads, 2) mass_kernel(Args A) {
     using Wn = Win<NC>;
     constexpr int NB = Wn::NB, ACC_ROW = Wn::ACC_ROW, ACC_FLOATS = Wn::ACC_FLOATS;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -282,8 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
         const int by = (int)((blk / A.nb[0]) % A.nb[1]);
         const int bz = (int)(blk / ((long long)A.nb[0] * A.nb[1]));
         __syncthreads();  // previous block's flush finished with cstart/ccount
-        if (tid < 64) {
-            const int cx = bx * BC + (tid & 3), cy = by * BC + ((tid >> 2) & 3), cz = bz * BC + (tid >> 4);
+        if (tid < NCELL) {
+            const int cx = bx * BCX + tid % BCX, cy = by * BCY + (tid / BCX) % BCY,
+                      cz = bz * BCZ + tid / (BCX * BCY);
             unsigned s = 0, c = 0;
             if (cx < A.N[0] && cy < A.N[1] && cz < A.N[2]) {
                 const long long cell = ((long long)cz * A.N[1] + cy) * A.N[0] + cx;
@@ -297,10 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
             }
             cstart[tid] = s;
             ccount[tid] = c;
-        } else if (tid < 64 + WN * WN) {
-            const int row = tid - 64;
-            const int gy = (by * BC + row % WN) % A.N[1], gz = (bz * BC + row / WN) % A.N[2];
-            const long long node = ((long long)gz * A.N[1] + gy) * A.N[0] + (bx * BC) % A.N[0];
+        } else if (tid < NCELL + NROWS) {
+            const int row = tid - NCELL;
+            const int gy = (by * BCY + row % WNY) % A.N[1], gz = (bz * BCZ + row / WNY) % A.N[2];
+            const long long node = ((long long)gz * A.N[1] + gy) * A.N[0] + (bx * BCX) % A.N[0];
             rsh[row] = (int)((node * NB) & 3);
         }
         __syncthreads();
@@ -312,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
         Raw raw = load_raw<NC>(A, bt[jme], kme);
         while (any) {
             const Batch mine = bt[jme];
-            const int cx = bx * BC + (mine.ci & 3), cy = by * BC + ((mine.ci >> 2) & 3),
-                      cz = bz * BC + (mine.ci >> 4);
+            const int cx = bx * BCX + mine.ci % BCX, cy = by * BCY + (mine.ci / BCX) % BCY,
+                      cz = bz * BCZ + mine.ci / (BCX * BCY);
             float W[8], s[NC];
             prepare<NC>(A, raw, cx, cy, cz, half == 0, W, s);
 
@@ -445,9 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
                     for (int h = 0; h < 2; ++h) {
                         if (dj[h] < 0) continue;
                         const int ci = bt[dj[h]].ci;
-                        const int nx = (ci & 3) + (a & 1), ny = ((ci >> 2) & 3) + ((a >> 1) & 1),
-                                  nz = (ci >> 4) + (a >> 2);
-                        const int wr = nz * WN + ny;
+                        const int nx = ci % BCX + (a & 1), ny = (ci / BCX) % BCY + ((a >> 1) & 1),
+                                  nz = ci / (BCX * BCY) + (a >> 2);
+                        const int wr = nz * WNY + ny;
                         float *row = acc + wr * ACC_ROW + rsh[wr] + nx * NB + c;
 #pragma unroll
                         for (int nn = 0; nn < 8; ++nn) {
@@ -469,14 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
         // ---- flush the node window: each row of 5 node blocks is contiguous in M ----
         tc::fence_proxy_async_smem();  // the window's shared-memory reductions, for the TMA
         __syncthreads();
-        for (int row = 0; row < WN * WN; ++row) {
-            const int gy = (by * BC + row % WN) % A.N[1];
-            const int gz = (bz * BC + row / WN) % A.N[2];
+        for (int row = 0; row < NROWS; ++row) {
+            const int gy = (by * BCY + row % WNY) % A.N[1];
+            const int gz = (bz * BCZ + row / WNY) % A.N[2];
             const float *src = acc + row * ACC_ROW + rsh[row];
             int nx0 = 0;
-            while (nx0 < WN) {
-                const int gx0 = (bx * BC + nx0) % A.N[0];
-                int len = WN - nx0;
+            while (nx0 < WNX) {
+                const int gx0 = (bx * BCX + nx0) % A.N[0];
+                int len = WNX - nx0;
                 if (gx0 + len > A.N[0]) len = A.N[0] - gx0;  // the row wraps at the x boundary
                 float *dst = A.M + (((long long)gz * A.N[1] + gy) * A.N[0] + gx0) * NB;
                 const float *sp = src + nx0 * NB;
@@ -524,7 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1) mass_kernel(Args A) {
 
 template <int MODE, int NC>
 size_t smem_bytes() {
-    return Op<MODE, NC>::STAGING + Win<NC>::ACC_BYTES + 64 * 8 + 32 * 4 + 16;
+    const size_t used = Op<MODE, NC>::STAGING + Win<NC>::ACC_BYTES + 64 * 8 + 32 * 4 + 16;
+    const size_t reads = Op<MODE, NC>::READ_END;
+    return used > reads ? used : reads;
 }
 
 template <int MODE, int NC>
@@ -533,7 +548,8 @@ pcg_status launch(const Args &A, cudaStream_t s) {
     PCG_CHECK_CUDA(cudaFuncSetAttribute(mass_kernel<MODE, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)smem));
     const long long nblocks = (long long)A.nb[0] * A.nb[1] * A.nb[2];
-    const long long grid = nblocks < num_sms() ? nblocks : num_sms();
+    const long long cap = 2ll * num_sms();  // two CTAs per SM
+    const long long grid = nblocks < cap ? nblocks : cap;
     static const char *const names[2][3] = {
         {"mass_matrix_tf32", "mass_matrix_bf16", "mass_matrix_simt"},
         {"mass_scalar_tf32", "mass_scalar_bf16", "mass_scalar_simt"}};
@@ -578,7 +594,7 @@ pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64
     Args A{};
     for (int mu = 0; mu < 3; ++mu) {
         A.N[mu] = grid[mu];
-        A.nb[mu] = (grid[mu] + BC - 1) / BC;
+        A.nb[mu] = (grid[mu] + (mu == 0 ? BCX : mu == 1 ? BCY : BCZ) - 1) / (mu == 0 ? BCX : mu == 1 ? BCY : BCZ);
     }
     A.ncells = ncells;
     if (n > 0) {
