@@ -474,7 +474,8 @@ def cic1d_workload(pcg, steps, warmup, dist):
                                     "M_particle_steps_per_s": round(n * 50 / (us * 1e-6) / 1e6, 1)}
         del x0, v, tg, g
     out["note"] = ("N=2000: latency-bound, one cluster launch (+1 for the gradient); N=10^7: 80 MB of "
-                   "input, resident in L2 between calls, bound by the fp32 screen of 5e8 pairs")
+                   "input, resident in L2 between calls; ~4.5 screened steps per particle (those near its "
+                   "window crossings), fp64 decisions on the ~5e6 selected pairs")
     return out
 
 

@@ -158,3 +158,22 @@ def test_grad_overwrites_stale_output():
     g = host(g)
     assert np.isfinite(g).all()
     assert np.abs(g - gr).max() <= DEPOSIT_TOL * np.abs(gr).max()
+
+
+@pytest.mark.parametrize("n", [3000, 40000])
+def test_particles_moving_with_the_window(n):
+    """Velocities near 1/(T dt), where a particle keeps pace with the window and
+    stays selected for many consecutive steps, mixed with ordinary and fast
+    ones: the candidate-step enumeration and its fallback must both cover
+    every step the fp64 test selects."""
+    pcg = need_gpu()
+    rng = np.random.default_rng(n)
+    T, dt, hw = 50, 0.01, 0.005
+    x0 = rng.random(n).astype(np.float32)
+    v = np.where(rng.random(n) < 0.5, 1.0 / (T * dt) + rng.normal(0, 0.02, n), rng.normal(0, 0.1, n))
+    v[: n // 10] = 1.0 / (T * dt)
+    v[n // 10: n // 5] = rng.normal(0, 30.0, n // 5 - n // 10)
+    v = v.astype(np.float32)
+    target = rng.random(1024).astype(np.float32)
+    H, L, g = _run_grad(pcg, x0, v, target, T, dt, hw)
+    _check_grad(H, L, g, x0, v, target, T, dt, hw)
