@@ -64,6 +64,8 @@ def _load():
             lib.oracle_deposit_current.argtypes = [i32, vp, i32, i64, vp, vp, vp, vp]
             lib.oracle_mass_matrix_scalar.restype = i64
             lib.oracle_mass_matrix_scalar.argtypes = [vp, i64, vp, vp, vp]
+            lib.oracle_mass_matrix_tsc.restype = i64
+            lib.oracle_mass_matrix_tsc.argtypes = [vp, i64, vp, vp, vp, vp]
             lib.oracle_deposit_zigzag.restype = i64
             lib.oracle_deposit_zigzag.argtypes = [vp, i64, vp, vp, vp, dbl, vp]
             lib.oracle_alpha.restype = None
@@ -190,6 +192,21 @@ def mass_matrix(grid, pos, wq, omega):
     ninv = lib.oracle_mass_matrix(_ptr(g), wq.size, _ptr_array(pos), _ptr(wq),
                                   _ptr_array(omega), _ptr(M))
     return M.reshape(tuple(reversed(grid)) + (27, 3, 3)), int(ninv)
+
+
+def mass_matrix_tsc(grid, pos, wq, omega):
+    """M (float64[Nz, Ny, Nx, 125, 3, 3]) for second-order (TSC) shapes, every
+    offset in {-2..2}^3 kept (Pennati & Markidis, Sec. 2.3, 3.3-3.4); returns
+    (M, n_invalid).  Every grid edge must be >= 5."""
+    lib = _load()
+    assert all(N >= 5 for N in grid)
+    pos = [_f32(p) for p in pos]
+    omega = [_f32(o) for o in omega]
+    wq = _f32(wq)
+    g = np.array(grid, dtype=np.int32)
+    M = np.zeros(int(np.prod(grid)) * 1125, dtype=np.float64)
+    ninv = lib.oracle_mass_matrix_tsc(_ptr(g), wq.size, _ptr_array(pos), _ptr(wq), _ptr_array(omega), _ptr(M))
+    return M.reshape(tuple(reversed(grid)) + (125, 3, 3)), int(ninv)
 
 
 def mass_matrix_scalar(grid, pos, w):

@@ -396,6 +396,50 @@ int64_t oracle_mass_matrix(const int32_t *grid, int64_t n,
     return n_invalid;
 }
 
+/* Mass matrix with second-order (TSC) B-splines (Pennati & Markidis, Sec. 2.3
+ * Eq. (12) and the base-offset rule: a coordinate with fractional part < 1/2
+ * uses nodes j-1..j+1, else j..j+2; Sec. 3.3: particles of a cell with the same
+ * node set form a support group, up to 8 per cell; Sec. 3.4: displacements in
+ * {-2..2}^3, 125 offsets).  M^{ij}_{gg'} = sum_p w_p alpha_p^{ij} W_pg W_pg',
+ * stored with every offset: M[g][o][i][j], o = (dz+2)*25 + (dy+2)*5 + (dx+2)
+ * for g' = g + (dx,dy,dz) (periodic), double[ncells][125][9], overwritten.
+ * Every grid edge must be >= 5.  Returns the particles skipped for a
+ * coordinate outside [0, N). */
+int64_t oracle_mass_matrix_tsc(const int32_t *grid, int64_t n, const float *const *pos, const float *wq,
+                               const float *const *omega, double *M) {
+    int32_t Nx = grid[0], Ny = grid[1], Nz = grid[2];
+    int64_t ncells = (int64_t)Nx * Ny * Nz;
+    memset(M, 0, sizeof(double) * 1125 * (size_t)ncells);
+    int64_t n_invalid = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        double x[3] = {pos[0][p], pos[1][p], pos[2][p]};
+        if (!in_domain(x[0], Nx) || !in_domain(x[1], Ny) || !in_domain(x[2], Nz)) {
+            ++n_invalid;
+            continue;
+        }
+        int64_t first[3];
+        double wt[3][3];
+        for (int mu = 0; mu < 3; ++mu) axis_support(2, x[mu], &first[mu], wt[mu]);
+        double om[3] = {omega[0][p], omega[1][p], omega[2][p]};
+        double alpha[9];
+        oracle_alpha(om, alpha);
+        for (int a = 0; a < 27; ++a) {
+            int ax = a % 3, ay = (a / 3) % 3, az = a / 9;
+            double Wa = wt[0][ax] * wt[1][ay] * wt[2][az];
+            int64_t g = (mod_floor(first[2] + az, Nz) * Ny + mod_floor(first[1] + ay, Ny)) * Nx
+                        + mod_floor(first[0] + ax, Nx);
+            for (int b = 0; b < 27; ++b) {
+                int bx = b % 3, by = (b / 3) % 3, bz = b / 9;
+                double Wb = wt[0][bx] * wt[1][by] * wt[2][bz];
+                int o = (bz - az + 2) * 25 + (by - ay + 2) * 5 + (bx - ax + 2);
+                double *blk = M + ((size_t)g * 125 + (size_t)o) * 9;
+                for (int ij = 0; ij < 9; ++ij) blk[ij] += (double)wq[p] * alpha[ij] * Wa * Wb;
+            }
+        }
+    }
+    return n_invalid;
+}
+
 /* Scalar mass matrix (Pennati & Markidis, Sec. 2.1 after Eq. (6): the scalar
  * case s_p^{ij} = q_p delta^{ij}, e.g. the MPM mass matrix, one component per
  * node pair): M_{gg'} = sum_p w_p W_pg W_pg' with CIC shapes, stored by stencil

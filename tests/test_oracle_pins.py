@@ -613,3 +613,78 @@ def test_zigzag_invalid_moves_skipped_and_counted():
     J, ninv = oracle.deposit_zigzag(grid, a, b, np.concatenate([q, np.ones(4, np.float32)]), dt)
     assert ninv == 4
     assert np.array_equal(J, J_ok)
+
+
+# ---------------------------------------------------------------------------
+# TSC (second-order) mass matrix (Pennati & Markidis, Sec. 2.3, 3.3-3.4):
+# the dense W S W^T with W from the convolution-built quadratic spline
+# ---------------------------------------------------------------------------
+def _dense_mass_order(grid, pos, wq, omega, order):
+    Nx, Ny, Nz = grid
+    ng = Nx * Ny * Nz
+    n = len(wq)
+    gz, gy, gx = np.meshgrid(np.arange(Nz), np.arange(Ny), np.arange(Nx), indexing="ij")
+    W = np.zeros((ng, n))
+    for p in range(n):
+        Wp = (_phi(order, _minimg(float(pos[0][p]) - gx, Nx)) * _phi(order, _minimg(float(pos[1][p]) - gy, Ny))
+              * _phi(order, _minimg(float(pos[2][p]) - gz, Nz)))
+        W[:, p] = Wp.ravel()
+    S = np.zeros((3, 3, n))
+    for p in range(n):
+        w = np.array([float(omega[c][p]) for c in range(3)])
+        S[:, :, p] = float(wq[p]) * np.linalg.solve(np.eye(3) + _cross_matrix(w), np.eye(3))
+    return np.einsum("gp,ijp,hp->ijgh", W, S, W)
+
+
+def _offset_layout_125(Md, grid):
+    Nx, Ny, Nz = grid
+    ng = Nx * Ny * Nz
+    out = np.zeros((ng, 125, 3, 3))
+    for g in range(ng):
+        x, y, z = g % Nx, (g // Nx) % Ny, g // (Nx * Ny)
+        for dz in range(-2, 3):
+            for dy in range(-2, 3):
+                for dx in range(-2, 3):
+                    h = (((z + dz) % Nz) * Ny + (y + dy) % Ny) * Nx + (x + dx) % Nx
+                    out[g, (dz + 2) * 25 + (dy + 2) * 5 + (dx + 2)] = Md[:, :, g, h]
+    return out
+
+
+@pytest.mark.parametrize("grid", [(5, 6, 5), (7, 5, 6)])
+def test_tsc_mass_matrix_dense_product(grid):
+    rng = np.random.default_rng(sum(grid) + 200)
+    n = 25
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    # fractional parts either side of 1/2, on a node, at the top edge (wraps)
+    pos[0][0], pos[1][0], pos[2][0] = 1.5, 2.25, 3.75
+    pos[0][1] = np.float32(grid[0]) - np.float32(1e-5)
+    pos[2][2] = 0.0
+    wq = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    omega = [rng.normal(0, 0.6, n).astype(np.float32) for _ in range(3)]
+    M, ninv = oracle.mass_matrix_tsc(grid, pos, wq, omega)
+    assert ninv == 0
+    want = _offset_layout_125(_dense_mass_order(grid, pos, wq, omega, 2), grid)
+    assert np.abs(M.reshape(-1, 125, 3, 3) - want).max() <= 1e-12 * np.abs(want).max()
+
+
+def test_tsc_mass_matrix_symmetry_and_groups():
+    """Each component block is symmetric in (g, g') (Eq. (11)); a particle's 27
+    nodes follow the base-offset rule, so a cell holds at most 8 node sets."""
+    grid = (6, 5, 7)
+    rng = np.random.default_rng(31)
+    n = 300
+    pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+    wq = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    omega = [rng.normal(0, 0.6, n).astype(np.float32) for _ in range(3)]
+    M, _ = oracle.mass_matrix_tsc(grid, pos, wq, omega)
+    for o in range(125):
+        dz, dy, dx = o // 25 - 2, (o // 5) % 5 - 2, o % 5 - 2
+        mirrored = np.roll(M[:, :, :, 124 - o], shift=(-dz, -dy, -dx), axis=(0, 1, 2))
+        assert np.abs(M[:, :, :, o] - mirrored).max() <= 1e-12 * np.abs(M).max()
+    firsts = set()
+    for p in range(n):
+        cell = tuple(int(np.floor(pos[mu][p])) for mu in range(3))
+        f = tuple(oracle.axis_support(2, float(pos[mu][p]))[0] - cell[mu] for mu in range(3))
+        assert all(v in (-1, 0) for v in f)
+        firsts.add(f)
+    assert len(firsts) == 8
