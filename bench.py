@@ -491,6 +491,29 @@ def mass_workload(pcg, steps, warmup, dist, peaks, traffic, edge=64):
     return res
 
 
+def tsc_workload(pcg, steps, warmup, dist, peaks, traffic, edge=32):
+    """Second-order (TSC) ECSIM mass matrix on CUDA cores, 125 offsets x 3x3 per node."""
+    import torch
+    import synth
+    d = synth.mass3d(grid=(edge, edge, edge))
+    grid, n = d["grid"], d["n"]
+    dev = lambda a: torch.from_numpy(a).cuda()
+    dp = [dev(p) for p in d["pos"]]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(d["w"])] + [dev(o) for o in d["omega"]])
+    M = torch.empty(tuple(reversed(grid)) + (125, 3, 3), dtype=torch.float32, device="cuda")
+    step = lambda: pcg.assemble_mass_matrix(grid, out[:3], out[3], out[4:7], offs, precision="simt", M=M, order=2)
+    step()
+    ms = time_steps(step, steps, warmup, dist, torch.cuda.current_stream(), pcg=pcg)
+    timed = pcg.profile_collect()
+    ent = roofline_entry("mass_tsc_simt", timed, n * 28 + M.numel() * 4, peaks["hbm_gbs"], traffic, n)
+    res = {"workload": f"mass3d TSC {edge}^3 x 64 ppc (125 offsets x 3x3 blocks, CUDA cores)", "particles": n,
+           "ms_per_call": round(ms / steps, 4), "M_particles_per_s": round(n / (ms / steps * 1e-3) / 1e6, 1),
+           "roofline": ent, "useful_tflops": round(n * 27 * 27 * 9 * 2 / (ent["avg_ms"] * 1e-3) / 1e12, 2)}
+    del dp, out, offs, M
+    torch.cuda.empty_cache()
+    return res
+
+
 def cic1d_workload(pcg, steps, warmup, dist):
     """The 1D windowed CIC histogram + loss, and its gradient dL/dx0, at the
     pages' N = 2000 and at N = 10^7 (the size their gradient timings use)."""
@@ -582,6 +605,7 @@ def run_gpu(args):
                                  "stencil_updates_per_s": r4.get("stencil_updates_per_s")}
         del d4
         wl["mass3d_64"] = mass_workload(pcg, ks, kw, dist, peaks, traffic)
+        wl["mass3d_tsc_32"] = tsc_workload(pcg, ks, kw, dist, peaks, traffic)
         d5 = synth.zigzag3d()
         wl["zigzag3d_256"] = zigzag_workload(pcg, d5, ks, kw, dist, peaks, traffic)
         del d5
@@ -605,6 +629,8 @@ def run_only(args):
         out = mass_workload(pcg, args.steps, args.warmup, dist, peaks, traffic, edge=args.mass_grid)
     elif args.only == "cic1d":
         out = cic1d_workload(pcg, args.steps, args.warmup, dist)
+    elif args.only == "tsc":
+        out = tsc_workload(pcg, args.steps, args.warmup, dist, peaks, traffic, edge=args.mass_grid)
     elif args.only == "zigzag":
         out = zigzag_workload(pcg, synth.zigzag3d(grid=(args.zz_grid,) * 3), args.steps, args.warmup, dist, peaks,
                               traffic)
@@ -663,7 +689,7 @@ def main():
     ap.add_argument("--grid", type=int, default=256, help="edge of the headline workload's grid (256 = full size)")
     ap.add_argument("--main-only", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--only", choices=["mass", "quad", "cic2d", "cic1d", "zigzag"], default=None,
+    ap.add_argument("--only", choices=["mass", "quad", "cic2d", "cic1d", "zigzag", "tsc"], default=None,
                     help="time one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--mass-grid", type=int, default=64, help="edge of the mass-matrix grid")
     ap.add_argument("--zz-grid", type=int, default=256, help="edge of the zigzag grid (--only zigzag)")

@@ -294,7 +294,8 @@ PCG_API pcg_status pcg_deposit_zigzag(const int32_t *grid, int32_t tile, int64_t
                                       size_t workspace_bytes, void *stream);
 
 /* -------------------------------------------------------------------------
- * ECSIM block mass matrix with first-order (CIC) B-splines.
+ * ECSIM block mass matrix with first-order (CIC) or second-order (TSC)
+ * B-splines.
  * Defined by Pennati & Markidis, Sec. 2.1, Eqs. (4)-(6):
  *   M^{ij}_{g g'} = sum_p s_p^{ij} W_pg W_pg',  s_p = w_p alpha_p,
  *   alpha_p = (I - C(omega_p) + omega_p omega_p^T) / (1 + |omega_p|^2),
@@ -304,15 +305,22 @@ PCG_API pcg_status pcg_deposit_zigzag(const int32_t *grid, int32_t tile, int64_t
  * particles, accumulated in place), and stored by stencil offset as in Sec. 3.4
  * with all 27 offsets kept.
  *
- * Output layout: M[g][o][i][j], g the row node, o = (dz+1)*9 + (dy+1)*3 + (dx+1)
- * the offset of the column node g' = g + (dx, dy, dz) (periodic), i, j the
- * tensor component; float[ncells][27][3][3].
+ * Output layout, order 1: M[g][o][i][j], g the row node,
+ * o = (dz+1)*9 + (dy+1)*3 + (dx+1) the offset of the column node
+ * g' = g + (dx, dy, dz) (periodic), i, j the tensor component;
+ * float[ncells][27][3][3].
+ * Order 2 (Sec. 2.3: per axis nodes j-1..j+1 when the fractional part is
+ * < 1/2, else j..j+2; Sec. 3.3-3.4: up to 8 support groups per cell,
+ * displacements in {-2..2}^3): o = (dz+2)*25 + (dy+2)*5 + (dx+2);
+ * float[ncells][125][3][3], every offset kept.
  *
- *   grid       HOST int32[3], each >= 3 (so that the 27 offsets are distinct).
- *   order      1.
+ *   grid       HOST int32[3], each >= 3 for order 1 and >= 5 for order 2 (so
+ *              that the offsets are distinct nodes).
+ *   order      1 or 2.
  *   precision  0 = TF32 tensor cores (tcgen05.mma kind::tf32, fp32 accumulate
  *              in tensor memory); 1 = BF16 tensor cores (kind::f16); 2 = fp32
- *              CUDA cores (no tensor cores; the A/B baseline).
+ *              CUDA cores (no tensor cores; the A/B baseline).  Order 2 runs on
+ *              CUDA cores only: precision 0 or 1 returns PCG_ERR_UNSUPPORTED.
  *   n          number of particles.
  *   pos        HOST array of 3 device float[n]; w device float[n] (q^2/m);
  *   omega      HOST array of 3 device float[n] (omega = beta_s B(x_p) / c).
@@ -321,7 +329,8 @@ PCG_API pcg_status pcg_deposit_zigzag(const int32_t *grid, int32_t tile, int64_t
  *              cell_offsets[c+1]).  A particle whose position is not inside the
  *              cell it is listed under is still deposited correctly (through
  *              global atomics) and flagged with PCG_FLAG_CELL_MISMATCH.
- *   M          device float[ncells * 243], output (overwritten).
+ *   M          device float[ncells * 243] (order 1) or [ncells * 1125]
+ *              (order 2), 16-byte aligned, output (overwritten).
  *   stats      device pcg_stats or NULL.
  *   workspace  pcg_assemble_mass_matrix_workspace_size() bytes (currently 0).
  */

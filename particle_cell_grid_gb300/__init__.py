@@ -243,8 +243,9 @@ def assemble_mass_matrix_workspace_size(grid, n) -> int:
 
 
 def assemble_mass_matrix(grid, pos, w, omega, cell_offsets, precision="tf32", M=None, stats=None,
-                         workspace=None, stream=None):
-    """M[g][o][i][j] (float32[Nz, Ny, Nx, 27, 3, 3]) from cell-sorted particles."""
+                         workspace=None, stream=None, order=1):
+    """M[g][o][i][j] from cell-sorted particles: float32[Nz, Ny, Nx, 27, 3, 3] for
+    order 1 (CIC), float32[Nz, Ny, Nx, 125, 3, 3] for order 2 (TSC, CUDA cores)."""
     n = w.numel()
     for i, t in enumerate(pos):
         _dev(t, torch.float32, f"pos[{i}]")
@@ -253,11 +254,11 @@ def assemble_mass_matrix(grid, pos, w, omega, cell_offsets, precision="tf32", M=
     _dev(w, torch.float32, "w")
     _dev(cell_offsets, None, "cell_offsets")
     dev = w.device
-    shape = tuple(int(N) for N in reversed(grid)) + (27, 3, 3)
+    shape = tuple(int(N) for N in reversed(grid)) + ((27 if order == 1 else 125), 3, 3)
     M = torch.empty(shape, dtype=torch.float32, device=dev) if M is None else _dev(M, torch.float32, "M")
     ws = _workspace(assemble_mass_matrix_workspace_size(grid, n), dev, workspace)
     prec = PRECISION[precision] if isinstance(precision, str) else int(precision)
-    st = _lib.load().pcg_assemble_mass_matrix(_grid_arr(grid), 1, prec, n, _ptr_arr(pos, 3), _ptr(w),
+    st = _lib.load().pcg_assemble_mass_matrix(_grid_arr(grid), int(order), prec, n, _ptr_arr(pos, 3), _ptr(w),
                                               _ptr_arr(omega, 3), _ptr(cell_offsets), _ptr(M), _ptr(stats),
                                               _ptr(ws), _ws_bytes(ws), _stream(stream))
     check(st, "pcg_assemble_mass_matrix")

@@ -569,6 +569,12 @@ extern "C" pcg_status pcg_assemble_mass_matrix_workspace_size(const int32_t *gri
 }
 
 namespace pcg {
+namespace tsc {
+// mass_tsc.cu: the second-order (TSC) assembly on CUDA cores; M zeroed by the caller.
+pcg_status launch_mass_tsc(const int32_t *grid, long long ncells, long long n, const float *const *pos,
+                           const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
+                           unsigned *flags, cudaStream_t s);
+}  // namespace tsc
 namespace mm {
 namespace {
 
@@ -577,13 +583,16 @@ template <int NC>
 pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64_t n, const float *const *pos,
                     const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
                     pcg_stats *stats, void *stream) {
-    if (grid == nullptr || order != 1 || n < 0 || n >= 0xffffffffll) return PCG_ERR_INVALID_ARG;
+    if (grid == nullptr || n < 0 || n >= 0xffffffffll) return PCG_ERR_INVALID_ARG;
+    if (order != 1 && !(order == 2 && NC == 9)) return PCG_ERR_INVALID_ARG;
     if (precision < 0 || precision > 2) return PCG_ERR_INVALID_ARG;
+    const int min_edge = order == 2 ? 5 : 3;  // the 27 or 125 offsets must be distinct nodes
     long long ncells = 1;
     for (int mu = 0; mu < 3; ++mu) {
-        if (grid[mu] < 3 || grid[mu] > (1 << 20)) return PCG_ERR_INVALID_ARG;
+        if (grid[mu] < min_edge || grid[mu] > (1 << 20)) return PCG_ERR_INVALID_ARG;
         ncells *= grid[mu];
     }
+    if (order == 2 && precision != 2) return PCG_ERR_UNSUPPORTED;  // TSC: CUDA cores only
     if (ncells >= (1ll << 31)) return PCG_ERR_INVALID_ARG;
     if (M == nullptr || !aligned16(M) || cell_offsets == nullptr) return PCG_ERR_INVALID_ARG;
     if (n > 0 && (pos == nullptr || w == nullptr || pos[0] == nullptr || pos[1] == nullptr || pos[2] == nullptr))
@@ -613,8 +622,9 @@ pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64
     A.M = M;
     A.flags = stats ? &stats->error_flags : nullptr;
     cudaStream_t s = as_stream(stream);
-    pcg_status st = zero_f32(M, (size_t)ncells * Win<NC>::NB, s);
+    pcg_status st = zero_f32(M, (size_t)ncells * (order == 2 ? 1125 : Win<NC>::NB), s);
     if (st != PCG_OK || n == 0) return st;
+    if (order == 2) return tsc::launch_mass_tsc(grid, ncells, n, pos, w, omega, cell_offsets, M, A.flags, s);
     switch (precision) {
         case 0: return launch<TF32, NC>(A, s);
         case 1: return launch<BF16, NC>(A, s);

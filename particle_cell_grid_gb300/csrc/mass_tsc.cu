@@ -1,0 +1,228 @@
+// mass_tsc.cu -- ECSIM block mass matrix with second-order (TSC) B-splines, on
+// CUDA cores.
+//
+// Method: Pennati & Markidis, "Mass Matrix Assembly on Tensor Cores for
+// Implicit Particle-In-Cell Methods".
+//   Eqs. (4)-(6): M^{ij}_{gg'} = sum_p w_p alpha_p^{ij} W_pg W_pg'.
+//   Sec. 2.3:     quadratic B-spline weights per axis; a coordinate whose
+//                 fractional part is < 1/2 uses nodes j-1..j+1, else j..j+2.
+//   Sec. 3.3:     particles of one cell with the same node set form a support
+//                 group (up to 8); the alternative the section names, one
+//                 product over the union of the groups' nodes with zero weights
+//                 outside each particle's own 27, is what this kernel does.
+//   Sec. 3.4:     displacements in {-2..2}^3: 125 offsets per node, all kept.
+//
+// GB300 design (first version, CUDA cores).  One 512-thread CTA per cell: the
+// union of the supports of the cell's particles is the 4x4x4 node block
+// starting one node below the cell.  Thread (a, h) owns union node a (0..63)
+// and the 8 partner nodes b = 8h..8h+7, i.e. 72 accumulators (8 pairs x 9
+// components) in registers, for every particle of the cell.  Particles are
+// staged 64 at a time: their per-node weights (64 x 64 floats, zero outside
+// their 27 nodes) and coefficients w alpha in shared memory.  At the end of the
+// cell every pair within +-2 nodes per axis is added to M with one global
+// reduction per component; the cells are walked in order so that the rows they
+// share stay in L2.
+#include "common.cuh"
+
+namespace pcg {
+namespace tsc {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int KB = 64;     // particles per staged batch
+constexpr int NU = 64;     // union nodes (4 x 4 x 4)
+
+struct Args {
+    int N[3];
+    long long ncells;
+    const float *x, *y, *z, *w, *ox, *oy, *oz;
+    const uint32_t *offs;
+    long long n;
+    float *M;
+    unsigned *flags;
+};
+
+__device__ __forceinline__ void alpha_w(float w, float ox, float oy, float oz, float (&s)[9]) {
+    const float n2 = ox * ox + oy * oy + oz * oz;
+    const float f = w / (1.f + n2);
+    s[0] = f * (1.f + ox * ox);
+    s[1] = f * (oz + ox * oy);
+    s[2] = f * (-oy + ox * oz);
+    s[3] = f * (-oz + oy * ox);
+    s[4] = f * (1.f + oy * oy);
+    s[5] = f * (ox + oy * oz);
+    s[6] = f * (oy + oz * ox);
+    s[7] = f * (-ox + oz * oy);
+    s[8] = f * (1.f + oz * oz);
+}
+
+// Quadratic B-spline support of one coordinate: first node k - 1 with
+// k = i + (xi >= 1/2), and the weights at k-1, k, k+1 for s = x - k.
+__device__ __forceinline__ int tsc_axis(float x, float (&w)[3]) {
+    const int i = (int)x;  // x >= 0
+    const int k = i + (x - (float)i >= 0.5f ? 1 : 0);
+    const float s = x - (float)k;
+    const float a = 0.5f - s, b = 0.5f + s;
+    w[0] = 0.5f * a * a;
+    w[1] = 0.75f - s * s;
+    w[2] = 0.5f * b * b;
+    return k - 1;
+}
+
+__device__ __forceinline__ int wrapi(int i, int N) { return i >= N ? i - N : (i < 0 ? i + N : i); }
+
+// A particle not inside the cell it is listed under: all 27 x 27 x 9
+// contributions straight to global M.
+__device__ void particle_global(const Args &A, float x, float y, float z, float wq, float ox, float oy, float oz) {
+    float wx[3], wy[3], wz[3], s[9];
+    const int fx = tsc_axis(x, wx), fy = tsc_axis(y, wy), fz = tsc_axis(z, wz);
+    alpha_w(wq, ox, oy, oz, s);
+    for (int a = 0; a < 27; ++a) {
+        const int ax = a % 3, ay = (a / 3) % 3, az = a / 9;
+        const long long g = ((long long)wrapi(fz + az, A.N[2]) * A.N[1] + wrapi(fy + ay, A.N[1])) * A.N[0] +
+                            wrapi(fx + ax, A.N[0]);
+        const float Wa = wx[ax] * wy[ay] * wz[az];
+        for (int b = 0; b < 27; ++b) {
+            const int bx = b % 3, by = (b / 3) % 3, bz = b / 9;
+            const int o = (bz - az + 2) * 25 + (by - ay + 2) * 5 + (bx - ax + 2);
+            const float WW = Wa * wx[bx] * wy[by] * wz[bz];
+            for (int c = 0; c < 9; ++c) red_add_f32(A.M + (g * 125 + o) * 9 + c, s[c] * WW);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
+    __shared__ __align__(16) float Wt[KB][NU];  // per-node weights of the staged particles
+    __shared__ float S[KB][9];        // w alpha
+    __shared__ int rel[KB][3];        // first node relative to the union, -1 = skip
+    __shared__ float wax[KB][3][3];   // per-axis weights
+
+    const int tid = threadIdx.x;
+    const int a = tid >> 3, h = tid & 7;
+    const int ax = a & 3, ay = (a >> 2) & 3, az = a >> 4;
+
+    for (long long cell = blockIdx.x; cell < A.ncells; cell += gridDim.x) {
+        const int cx = (int)(cell % A.N[0]);
+        const int cy = (int)((cell / A.N[0]) % A.N[1]);
+        const int cz = (int)(cell / ((long long)A.N[0] * A.N[1]));
+        long long s0 = A.offs[cell], s1 = A.offs[cell + 1];
+        if (s1 < s0 || s1 > A.n) {
+            if (tid == 0 && A.flags) atomicOr(A.flags, PCG_FLAG_BAD_LAYOUT);
+            continue;  // uniform
+        }
+        if (s1 == s0) continue;
+
+        float acc[8][9];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int c = 0; c < 9; ++c) acc[j][c] = 0.f;
+
+        for (long long b0 = s0; b0 < s1; b0 += KB) {
+            const int len = (int)min((long long)KB, s1 - b0);
+            // ---- stage: per particle its union-relative support and coefficients ----
+            if (tid < len) {
+                const long long p = b0 + tid;
+                const float x = A.x[p], y = A.y[p], z = A.z[p];
+                const float wq = A.w[p], ox = A.ox[p], oy = A.oy[p], oz = A.oz[p];
+                const bool inside = x >= (float)cx && x < (float)(cx + 1) && y >= (float)cy &&
+                                    y < (float)(cy + 1) && z >= (float)cz && z < (float)(cz + 1);
+                if (inside) {
+                    float w3[3];
+                    rel[tid][0] = tsc_axis(x, w3) - (cx - 1);
+                    for (int e = 0; e < 3; ++e) wax[tid][0][e] = w3[e];
+                    rel[tid][1] = tsc_axis(y, w3) - (cy - 1);
+                    for (int e = 0; e < 3; ++e) wax[tid][1][e] = w3[e];
+                    rel[tid][2] = tsc_axis(z, w3) - (cz - 1);
+                    for (int e = 0; e < 3; ++e) wax[tid][2][e] = w3[e];
+                    float sv[9];
+                    alpha_w(wq, ox, oy, oz, sv);
+                    for (int c = 0; c < 9; ++c) S[tid][c] = sv[c];
+                } else {
+                    rel[tid][0] = -1;
+                    for (int c = 0; c < 9; ++c) S[tid][c] = 0.f;
+                    const bool ok = x >= 0.f && x < (float)A.N[0] && y >= 0.f && y < (float)A.N[1] && z >= 0.f &&
+                                    z < (float)A.N[2];
+                    if (ok) particle_global(A, x, y, z, wq, ox, oy, oz);
+                    if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
+                }
+            }
+            __syncthreads();
+            // ---- per-node weights, zero outside each particle's 27 nodes ----
+            for (int e = tid; e < KB * NU; e += kThreads) {
+                const int k = e / NU, nd = e % NU;
+                float W = 0.f;
+                if (k < len && rel[k][0] >= 0) {
+                    const int dx = (nd & 3) - rel[k][0], dy = ((nd >> 2) & 3) - rel[k][1], dz = (nd >> 4) - rel[k][2];
+                    if ((unsigned)dx < 3u && (unsigned)dy < 3u && (unsigned)dz < 3u)
+                        W = wax[k][0][dx] * wax[k][1][dy] * wax[k][2][dz];
+                }
+                Wt[k][nd] = W;
+            }
+            __syncthreads();
+            // ---- accumulate the 8 pairs (a, 8h + j) of this thread ----
+            for (int k = 0; k < len; ++k) {
+                const float wa = Wt[k][a];
+                if (wa == 0.f) continue;
+                const float4 p0 = *reinterpret_cast<const float4 *>(&Wt[k][8 * h]);
+                const float4 p1 = *reinterpret_cast<const float4 *>(&Wt[k][8 * h + 4]);
+                const float wb[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                float sv[9];
+#pragma unroll
+                for (int c = 0; c < 9; ++c) sv[c] = S[k][c];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float wab = wa * wb[j];
+#pragma unroll
+                    for (int c = 0; c < 9; ++c) acc[j][c] = fmaf(wab, sv[c], acc[j][c]);
+                }
+            }
+            __syncthreads();  // staging is reused by the next batch
+        }
+
+        // ---- flush the pairs within +-2 nodes per axis ----
+        const long long g = ((long long)wrapi(cz - 1 + az, A.N[2]) * A.N[1] + wrapi(cy - 1 + ay, A.N[1])) * A.N[0] +
+                            wrapi(cx - 1 + ax, A.N[0]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int b = 8 * h + j;
+            const int dx = (b & 3) - ax, dy = ((b >> 2) & 3) - ay, dz = (b >> 4) - az;
+            if (dx < -2 || dx > 2 || dy < -2 || dy > 2 || dz < -2 || dz > 2) continue;
+            const int o = (dz + 2) * 25 + (dy + 2) * 5 + (dx + 2);
+            float *dst = A.M + (g * 125 + o) * 9;
+#pragma unroll
+            for (int c = 0; c < 9; ++c)
+                if (acc[j][c] != 0.f) red_add_f32(dst + c, acc[j][c]);
+        }
+    }
+}
+
+}  // namespace
+
+// M (float[ncells][125][9]) must be zeroed by the caller; grid edges >= 5.
+pcg_status launch_mass_tsc(const int32_t *grid, long long ncells, long long n, const float *const *pos,
+                           const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
+                           unsigned *flags, cudaStream_t s) {
+    Args A{};
+    for (int mu = 0; mu < 3; ++mu) A.N[mu] = grid[mu];
+    A.ncells = ncells;
+    A.x = pos[0];
+    A.y = pos[1];
+    A.z = pos[2];
+    A.w = w;
+    A.ox = omega[0];
+    A.oy = omega[1];
+    A.oz = omega[2];
+    A.offs = cell_offsets;
+    A.n = n;
+    A.M = M;
+    A.flags = flags;
+    const long long cap = num_sms();
+    const long long ctas = ncells < cap ? ncells : cap;
+    prof::Mark mk("mass_tsc_simt", s);
+    mass_tsc_kernel<<<(unsigned)ctas, kThreads, 0, s>>>(A);
+    return launch_status();
+}
+
+}  // namespace tsc
+}  // namespace pcg

@@ -131,3 +131,59 @@ def test_scalar_variable_occupancy_and_mismatch(precision):
                                         precision=precision, stats=stats)
     assert rel_frobenius(host(M), Mr) <= TOL[precision]
     assert stats_dict(stats)["error_flags"] & 2
+
+
+# ---------------------------------------------------------------------------
+# second-order (TSC) matrix on CUDA cores: 125 offsets, support groups
+def _assemble_tsc(pcg, grid, pos, w, omega, precision="simt", stats=None):
+    dp = [dev(p) for p in pos]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(w)] + [dev(o) for o in omega])
+    return pcg.assemble_mass_matrix(grid, out[:3], out[3], out[4:7], offs, precision=precision, stats=stats,
+                                    order=2)
+
+
+@pytest.mark.parametrize("grid,ppc", [((5, 6, 5), 20), ((8, 8, 8), 64), ((7, 5, 9), 3)])
+def test_tsc_matches_oracle(grid, ppc):
+    pcg = need_gpu()
+    d = synth.mass3d(grid=grid, ppc=ppc, seed=sum(grid) + ppc + 7)
+    stats = pcg.new_stats()
+    M = host(_assemble_tsc(pcg, grid, d["pos"], d["w"], d["omega"], stats=stats))
+    Mr, _ = oracle.mass_matrix_tsc(grid, d["pos"], d["w"], d["omega"])
+    assert M.shape == Mr.shape
+    assert rel_frobenius(M, Mr) <= 1e-5
+    assert stats_dict(stats)["error_flags"] == 0
+
+
+def test_tsc_variable_occupancy_and_mismatch():
+    pcg = need_gpu()
+    grid = (6, 7, 5)
+    rng = np.random.default_rng(12)
+    ncell = int(np.prod(grid))
+    counts = rng.integers(0, 150, ncell)
+    counts[::4] = 0
+    cell = np.repeat(np.arange(ncell), counts)
+    n = cell.size
+    coords = [cell % grid[0], (cell // grid[0]) % grid[1], cell // (grid[0] * grid[1])]
+    perm = rng.permutation(n)
+    pos = [synth._inside_cell_f32(c, rng.random(n))[perm] for c in coords]
+    w = rng.uniform(0.5, 1.5, n).astype(np.float32)
+    omega = [rng.normal(0, 0.8, n).astype(np.float32) for _ in range(3)]
+    Mr, _ = oracle.mass_matrix_tsc(grid, pos, w, omega)
+    assert rel_frobenius(host(_assemble_tsc(pcg, grid, pos, w, omega)), Mr) <= 1e-5
+    # arrays that no longer match their cell layout: exact through the slow path, flagged
+    dp = [dev(p) for p in pos]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(w)] + [dev(o) for o in omega])
+    perm2 = np.random.default_rng(3).permutation(n)
+    arrs = [host(t)[perm2] for t in out]
+    stats = pcg.new_stats()
+    M = pcg.assemble_mass_matrix(grid, [dev(a) for a in arrs[:3]], dev(arrs[3]), [dev(a) for a in arrs[4:7]], offs,
+                                 precision="simt", stats=stats, order=2)
+    assert rel_frobenius(host(M), Mr) <= 1e-5
+    assert stats_dict(stats)["error_flags"] & 2
+
+
+def test_tsc_tensor_precisions_are_not_built():
+    pcg = need_gpu()
+    d = synth.mass3d(grid=(5, 5, 5), ppc=2, seed=4)
+    with pytest.raises(pcg.PcgError):
+        _assemble_tsc(pcg, d["grid"], d["pos"], d["w"], d["omega"], precision="tf32")
