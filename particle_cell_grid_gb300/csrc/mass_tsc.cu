@@ -19,8 +19,11 @@
 // components) in registers, for every particle of the cell.  Particles are
 // staged 64 at a time: their per-node weights (64 x 64 floats, zero outside
 // their 27 nodes) and coefficients w alpha in shared memory.  At the end of the
-// cell every pair within +-2 nodes per axis is added to M with one global
-// reduction per component; the cells are walked in order so that the rows they
+// cell every pair within +-2 nodes per axis is added to M: each thread's 4
+// partners along x are 4 consecutive offsets, i.e. a run of up to 36
+// consecutive floats of M, which goes out as 16-byte vector reductions between
+// a scalar head and tail: 9-12 reductions per run instead of 27-36 (32^3 x 64
+// ppc: 6.64 -> 5.80 ms).  The cells are walked in order so that the rows they
 // share stay in L2.
 #include "common.cuh"
 
@@ -88,6 +91,59 @@ __device__ void particle_global(const Args &A, float x, float y, float z, float 
             const float WW = Wa * wx[bx] * wy[by] * wz[bz];
             for (int c = 0; c < 9; ++c) red_add_f32(A.M + (g * 125 + o) * 9 + c, s[c] * WW);
         }
+    }
+}
+
+// One run of the flush: the partners bx = LO .. LO + L/9 - 1 of one row, i.e.
+// L consecutive floats of M starting at dst (= (g*125 + o)*9 floats into the
+// 16-byte-aligned M).  HEAD = floats up to the next 16-byte boundary: scalar
+// reductions for the head and the tail, 16-byte vector reductions between, so
+// every vector address is 16-byte aligned.  All-zero quads are skipped.
+template <int ROW, int LO, int L, int HEAD>
+__device__ __forceinline__ void flush_run(float *dst, const float (&acc)[8][9]) {
+#define PCG_TSC_V(e) acc[4 * ROW + LO + (e) / 9][(e) % 9]
+#pragma unroll
+    for (int e = 0; e < HEAD && e < L; ++e)
+        if (PCG_TSC_V(e) != 0.f) red_add_f32(dst + e, PCG_TSC_V(e));
+#pragma unroll
+    for (int e = HEAD; e + 4 <= L; e += 4) {
+        const float v0 = PCG_TSC_V(e), v1 = PCG_TSC_V(e + 1), v2 = PCG_TSC_V(e + 2), v3 = PCG_TSC_V(e + 3);
+        if (v0 != 0.f || v1 != 0.f || v2 != 0.f || v3 != 0.f) red_add_v4_f32(dst + e, v0, v1, v2, v3);
+    }
+#pragma unroll
+    for (int e = HEAD + (L - HEAD) / 4 * 4; e < L; ++e)
+        if (e >= HEAD && PCG_TSC_V(e) != 0.f) red_add_f32(dst + e, PCG_TSC_V(e));
+#undef PCG_TSC_V
+}
+
+// Row ROW (partners 4 ROW .. 4 ROW + 3 of this thread, one x-row of the union)
+// of node (ax, ay, az) into M: the partners within +-2 along x are bx = 0..2
+// (ax = 0), 1..3 (ax = 3) or 0..3.
+template <int ROW>
+__device__ __forceinline__ void flush_row(float *M, long long g, int ax, int ay, int az, int h,
+                                          const float (&acc)[8][9]) {
+    const int b0 = 8 * h + 4 * ROW;
+    const int dy = ((b0 >> 2) & 3) - ay, dz = (b0 >> 4) - az;
+    if (dy < -2 || dy > 2 || dz < -2 || dz > 2) return;
+    const int lo = ax == 3 ? 1 : 0;
+    const int o = (dz + 2) * 25 + (dy + 2) * 5 + (lo - ax + 2);
+    const long long start = (g * 125 + o) * 9;
+    const int head = (int)((4 - (start & 3)) & 3);
+    float *dst = M + start;
+    const int kind = ax == 0 ? 1 : (ax == 3 ? 2 : 0);  // 0: 4 partners from bx 0; 1: 3 from 0; 2: 3 from 1
+    switch (kind * 4 + head) {
+        case 0: flush_run<ROW, 0, 36, 0>(dst, acc); break;
+        case 1: flush_run<ROW, 0, 36, 1>(dst, acc); break;
+        case 2: flush_run<ROW, 0, 36, 2>(dst, acc); break;
+        case 3: flush_run<ROW, 0, 36, 3>(dst, acc); break;
+        case 4: flush_run<ROW, 0, 27, 0>(dst, acc); break;
+        case 5: flush_run<ROW, 0, 27, 1>(dst, acc); break;
+        case 6: flush_run<ROW, 0, 27, 2>(dst, acc); break;
+        case 7: flush_run<ROW, 0, 27, 3>(dst, acc); break;
+        case 8: flush_run<ROW, 1, 27, 0>(dst, acc); break;
+        case 9: flush_run<ROW, 1, 27, 1>(dst, acc); break;
+        case 10: flush_run<ROW, 1, 27, 2>(dst, acc); break;
+        default: flush_run<ROW, 1, 27, 3>(dst, acc); break;
     }
 }
 
@@ -180,20 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
             __syncthreads();  // staging is reused by the next batch
         }
 
-        // ---- flush the pairs within +-2 nodes per axis ----
+        // ---- flush the pairs within +-2 nodes per axis: two x-rows per thread ----
         const long long g = ((long long)wrapi(cz - 1 + az, A.N[2]) * A.N[1] + wrapi(cy - 1 + ay, A.N[1])) * A.N[0] +
                             wrapi(cx - 1 + ax, A.N[0]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int b = 8 * h + j;
-            const int dx = (b & 3) - ax, dy = ((b >> 2) & 3) - ay, dz = (b >> 4) - az;
-            if (dx < -2 || dx > 2 || dy < -2 || dy > 2 || dz < -2 || dz > 2) continue;
-            const int o = (dz + 2) * 25 + (dy + 2) * 5 + (dx + 2);
-            float *dst = A.M + (g * 125 + o) * 9;
-#pragma unroll
-            for (int c = 0; c < 9; ++c)
-                if (acc[j][c] != 0.f) red_add_f32(dst + c, acc[j][c]);
-        }
+        flush_row<0>(A.M, g, ax, ay, az, h, acc);
+        flush_row<1>(A.M, g, ax, ay, az, h, acc);
     }
 }
 
