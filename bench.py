@@ -569,7 +569,7 @@ def run_gpu(args):
         "metric": METRIC, "value": round(main["value"], 3), "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(main["ms_per_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded numpy PCG64; recipe in DESIGN.md)",
+        "data": "synthetic (seeded numpy PCG64 generators of synth/)",
         "config": {"workload": f"cic3d_drift {g}^3 x 16 ppc, CIC current deposit (sort + tiled deposit)",
                    "grid": [g, g, g], "particles": main["n"], "order": 1, "tile": 8, "halo": 2,
                    "step": "pcg_tile_sort + pcg_deposit_current", "parallelism": "replicas" if dist.world > 1 else "1 GPU",
