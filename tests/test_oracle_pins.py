@@ -688,3 +688,23 @@ def test_tsc_mass_matrix_symmetry_and_groups():
         assert all(v in (-1, 0) for v in f)
         firsts.add(f)
     assert len(firsts) == 8
+
+
+def test_zigzag_translation_covariance():
+    """Moving every particle (before and after its move) by whole cells along an
+    axis shifts J by the same number of nodes, periodically."""
+    grid, dt = (6, 5, 7), 0.5
+    x1, x2, q = _zigzag_moves(grid, 800, 21)
+    # positions on multiples of 2^-16, so that whole-cell shifts are exact in fp32
+    x1 = [(np.floor(a.astype(np.float64) * 65536) / 65536).astype(np.float32) for a in x1]
+    x2 = [(np.floor(a.astype(np.float64) * 65536) / 65536).astype(np.float32) for a in x2]
+    J, _ = oracle.deposit_zigzag(grid, x1, x2, q, dt)
+    for mu, shift in ((0, 2), (1, 4), (2, 3)):
+        N = grid[mu]
+        s1 = [a.copy() for a in x1]
+        s2 = [a.copy() for a in x2]
+        s1[mu] = ((x1[mu].astype(np.float64) + shift) % N).astype(np.float32)
+        s2[mu] = ((x2[mu].astype(np.float64) + shift) % N).astype(np.float32)
+        Js, ninv = oracle.deposit_zigzag(grid, s1, s2, q, dt)
+        assert ninv == 0
+        assert np.abs(Js - np.roll(J, shift, axis=3 - mu)).max() <= 1e-12 * np.abs(J).max()
