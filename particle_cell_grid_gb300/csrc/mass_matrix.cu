@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "mass_common.cuh"
 #include "tcgen05.cuh"
 
 namespace pcg {
@@ -115,19 +116,6 @@ struct Batch {
     unsigned start, len;
 };
 
-__device__ __forceinline__ void alpha_w(float w, float ox, float oy, float oz, float (&s)[9]) {
-    const float n2 = ox * ox + oy * oy + oz * oz;
-    const float f = w / (1.f + n2);
-    s[0] = f * (1.f + ox * ox);
-    s[1] = f * (oz + ox * oy);
-    s[2] = f * (-oy + ox * oz);
-    s[3] = f * (-oz + oy * ox);
-    s[4] = f * (1.f + oy * oy);
-    s[5] = f * (ox + oy * oz);
-    s[6] = f * (oy + oz * ox);
-    s[7] = f * (-ox + oz * oy);
-    s[8] = f * (1.f + oz * oz);
-}
 
 // Per-particle coefficients: w alpha (NC = 9) or w (NC = 1, the scalar case of Eq. (6)).
 template <int NC>

@@ -26,6 +26,7 @@
 // ppc: 6.64 -> 5.80 ms).  The cells are walked in order so that the rows they
 // share stay in L2.
 #include "common.cuh"
+#include "mass_common.cuh"
 
 namespace pcg {
 namespace tsc {
@@ -45,19 +46,6 @@ struct Args {
     unsigned *flags;
 };
 
-__device__ __forceinline__ void alpha_w(float w, float ox, float oy, float oz, float (&s)[9]) {
-    const float n2 = ox * ox + oy * oy + oz * oz;
-    const float f = w / (1.f + n2);
-    s[0] = f * (1.f + ox * ox);
-    s[1] = f * (oz + ox * oy);
-    s[2] = f * (-oy + ox * oz);
-    s[3] = f * (-oz + oy * ox);
-    s[4] = f * (1.f + oy * oy);
-    s[5] = f * (ox + oy * oz);
-    s[6] = f * (oy + oz * ox);
-    s[7] = f * (-ox + oz * oy);
-    s[8] = f * (1.f + oz * oz);
-}
 
 // Quadratic B-spline support of one coordinate: first node k - 1 with
 // k = i + (xi >= 1/2), and the weights at k-1, k, k+1 for s = x - k.
