@@ -232,9 +232,15 @@ PCG_API pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int32_t
  * given, and returns PCG_ERR_WORKSPACE above that (before launching anything).
  * The flat path (tile_offsets NULL) uses no scratch and has no such limit.
  *
+ * Arguments are checked exactly as pcg_deposit_current checks them, before the
+ * size limit and before any CUDA call.
+ *
  * It allocates nothing.  The first call made on a device looks up the array's
  * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  Every call shares the one array and
+ * first call before any stream capture.  The address is kept per device for the
+ * life of the process, which assumes the device's primary context (the one the
+ * CUDA runtime uses) is never reset: after cudaDeviceReset the kept address is
+ * stale, so do not call this entry point in a process that has reset the device.  Every call shares the one array and
  * each call rewrites every entry it reads, so nothing needs clearing between
  * calls; but calls whose kernels overlap on the GPU (different streams, no
  * ordering between them) race on the array and must not be issued.
@@ -328,10 +334,16 @@ PCG_API pcg_status pcg_deposit_zigzag(const int32_t *grid, int32_t tile, int64_t
  *              the particles listed under cell c are [cell_offsets[c],
  *              cell_offsets[c+1]).  A particle whose position is not inside the
  *              cell it is listed under is still deposited correctly (through
- *              global atomics) and flagged with PCG_FLAG_CELL_MISMATCH.
+ *              global atomics) and flagged with PCG_FLAG_CELL_MISMATCH.  Slots
+ *              [cell_offsets[ncells], n) (the sort's sentinel bin, or particles
+ *              appended after the sort) are deposited through global atomics
+ *              (the tail pass).
  *   M          device float[ncells * 243] (order 1) or [ncells * 1125]
  *              (order 2), 16-byte aligned, output (overwritten).
- *   stats      device pcg_stats or NULL.
+ *   stats      device pcg_stats or NULL: n_invalid counts the particles skipped
+ *              for a coordinate outside [0, N) or NaN, wherever they are listed
+ *              (a pcg_tile_sort into the same stats has counted those of its
+ *              sentinel bin already).
  *   workspace  pcg_assemble_mass_matrix_workspace_size() bytes (currently 0).
  */
 PCG_API pcg_status pcg_assemble_mass_matrix_workspace_size(const int32_t *grid, int64_t n, size_t *bytes);

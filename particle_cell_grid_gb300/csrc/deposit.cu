@@ -113,19 +113,18 @@ extern "C" pcg_status pcg_deposit_current_workspace_size(int32_t dim, const int3
     return PCG_OK;
 }
 
-extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int32_t order,
-                                          int32_t tile, int32_t halo, int32_t block, int64_t n,
-                                          const float *const *pos, const float *const *vel,
-                                          const float *q, const uint32_t *tile_offsets, float *J,
-                                          pcg_stats *stats, void *workspace,
-                                          size_t workspace_bytes, void *stream) {
-    using namespace pcg;
-    const bool tiled = tile_offsets != nullptr;
-    Geom g;
+namespace pcg {
+namespace {
+
+// Host checks shared by pcg_deposit_current and pcg_deposit_current_noalloc,
+// made before anything else (workspace, scratch lookup, launches).
+pcg_status check_current_args(int32_t dim, const int32_t *grid, int32_t order, int32_t tile, int32_t halo,
+                              int32_t block, int64_t n, const float *const *pos, const float *const *vel,
+                              const float *q, bool tiled, const float *J, Geom *g) {
     if (n < 0 || n >= 0xffffffffll) return PCG_ERR_INVALID_ARG;
     if (order != 1 && order != 2) return PCG_ERR_INVALID_ARG;
     if (tiled && (tile < 1 || tile > 64 || halo < 0)) return PCG_ERR_INVALID_ARG;
-    if (!geom_from(dim, grid, tiled ? tile : 1, &g)) return PCG_ERR_INVALID_ARG;
+    if (!geom_from(dim, grid, tiled ? tile : 1, g)) return PCG_ERR_INVALID_ARG;
     if (block != 0 && block != 128 && block != 256 && block != 512) return PCG_ERR_INVALID_ARG;
     if (J == nullptr || !aligned16(J)) return PCG_ERR_INVALID_ARG;
     if (n > 0) {
@@ -136,6 +135,25 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
             if (vel[c] == nullptr) return PCG_ERR_INVALID_ARG;
     }
     if (tiled && ((tile != 4 && tile != 8) || halo > 2)) return PCG_ERR_UNSUPPORTED;
+    return PCG_OK;
+}
+
+}  // namespace
+}  // namespace pcg
+
+extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int32_t order,
+                                          int32_t tile, int32_t halo, int32_t block, int64_t n,
+                                          const float *const *pos, const float *const *vel,
+                                          const float *q, const uint32_t *tile_offsets, float *J,
+                                          pcg_stats *stats, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    using namespace pcg;
+    const bool tiled = tile_offsets != nullptr;
+    Geom g;
+    {
+        const pcg_status st = check_current_args(dim, grid, order, tile, halo, block, n, pos, vel, q, tiled, J, &g);
+        if (st != PCG_OK) return st;
+    }
     const long long chunk = chunk_for(n);
     const long long nchunks = (n + chunk - 1) / chunk;
     const size_t need = tiled ? align_up((size_t)nchunks * sizeof(unsigned), 256) : 0;
@@ -234,7 +252,14 @@ extern "C" pcg_status pcg_deposit_current_noalloc(int32_t dim, const int32_t *gr
                                                   const uint32_t *tile_offsets, float *J,
                                                   pcg_stats *stats, void *stream) {
     using namespace pcg;
-    if (n < 0 || n >= 0xffffffffll) return PCG_ERR_INVALID_ARG;
+    {
+        // the same argument checks as pcg_deposit_current, before the size limit
+        // and before the scratch array's address is looked up
+        Geom g;
+        const pcg_status st = check_current_args(dim, grid, order, tile, halo, block, n, pos, vel, q,
+                                                 tile_offsets != nullptr, J, &g);
+        if (st != PCG_OK) return st;
+    }
     const long long chunk = chunk_for(n);
     const long long nchunks = (n + chunk - 1) / chunk;
     if (tile_offsets != nullptr && (size_t)nchunks > kNoAllocChunks) return PCG_ERR_WORKSPACE;

@@ -109,6 +109,7 @@ struct Args {
     long long n;
     float *M;
     unsigned *flags;
+    unsigned long long *n_invalid;
 };
 
 struct Batch {
@@ -188,7 +189,7 @@ __device__ __forceinline__ Raw load_raw(const Args &A, const Batch &b, int k) {
 // contributes zeros here.
 template <int NC>
 __device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int cy, int cz,
-                                        bool owner, float (&W)[8], float (&s)[NC]) {
+                                        bool owner, float (&W)[8], float (&s)[NC], unsigned &n_inv) {
     bool use = r.live;
     if (use) {
         const bool inside = r.x >= (float)cx && r.x < (float)(cx + 1) && r.y >= (float)cy &&
@@ -197,8 +198,12 @@ __device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int
             const bool ok = r.x >= 0.f && r.x < (float)A.N[0] && r.y >= 0.f && r.y < (float)A.N[1] &&
                             r.z >= 0.f && r.z < (float)A.N[2];
             if (owner) {  // once per particle, by one of the threads sharing it
-                if (ok) particle_global<NC>(A, r.x, r.y, r.z, r.w, r.ox, r.oy, r.oz);
-                if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
+                if (ok) {
+                    particle_global<NC>(A, r.x, r.y, r.z, r.w, r.ox, r.oy, r.oz);
+                    if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
+                } else {
+                    ++n_inv;  // outside the domain or NaN: skipped
+                }
             }
             use = false;
         }
@@ -223,6 +228,26 @@ __device__ __forceinline__ bool prepare(const Args &A, const Raw &r, int cx, int
     W[7] = fx * yz11;
     coeffs<NC>(r.w, r.ox, r.oy, r.oz, s);
     return true;
+}
+
+// The tail pass: slots [offs[ncells], n) are listed under no cell (the sort's
+// sentinel bin of invalid particles, or particles appended after the sort).
+// Valid ones go to M by the global path, invalid ones are counted.
+template <int NC>
+__device__ void tail_pass(const Args &A, unsigned &n_inv) {
+    const long long t0 = A.offs[A.ncells];
+    for (long long p = t0 + (long long)blockIdx.x * blockDim.x + threadIdx.x; p < A.n;
+         p += (long long)gridDim.x * blockDim.x) {
+        const float x = A.x[p], y = A.y[p], z = A.z[p];
+        const bool ok = x >= 0.f && x < (float)A.N[0] && y >= 0.f && y < (float)A.N[1] && z >= 0.f &&
+                        z < (float)A.N[2];
+        if (!ok) {
+            ++n_inv;
+            continue;
+        }
+        if (NC == 9) particle_global<NC>(A, x, y, z, A.w[p], A.ox[p], A.oy[p], A.oz[p]);
+        else particle_global<NC>(A, x, y, z, A.w[p], 0.f, 0.f, 0.f);
+    }
 }
 
 // The G batches starting at cursor (cur, cur_k); identical in every thread.
@@ -275,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 2) mass_kernel(Args A) {
     for (int i = tid; i < ACC_FLOATS; i += kThreads) acc[i] = 0.f;
     uint32_t phase = 0;
     bool timed_out = false;
+    unsigned n_inv = 0;
 
     const long long nblocks = (long long)A.nb[0] * A.nb[1] * A.nb[2];
     for (long long blk = blockIdx.x; blk < nblocks && !timed_out; blk += gridDim.x) {
@@ -316,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 2) mass_kernel(Args A) {
             const int cx = bx * BCX + mine.ci % BCX, cy = by * BCY + (mine.ci / BCX) % BCY,
                       cz = bz * BCZ + mine.ci / (BCX * BCY);
             float W[8], s[NC];
-            prepare<NC>(A, raw, cx, cy, cz, half == 0, W, s);
+            prepare<NC>(A, raw, cx, cy, cz, half == 0, W, s, n_inv);
 
             float d[2][8];   // this thread's rows of up to two batches
             int dj[2] = {-1, -1};
@@ -510,6 +536,8 @@ __global__ void __launch_bounds__(kThreads, 2) mass_kernel(Args A) {
         for (int i = tid; i < ACC_FLOATS; i += kThreads) acc[i] = 0.f;
     }
 
+    if (!timed_out) tail_pass<NC>(A, n_inv);
+    warp_add_u64(A.n_invalid, n_inv);
     if (tid == 0) tc::bulk_wait_all();
     if (MODE != SIMT) {
         // after a timeout, give the outstanding MMAs one more bounded wait
@@ -561,7 +589,7 @@ namespace tsc {
 // mass_tsc.cu: the second-order (TSC) assembly on CUDA cores; M zeroed by the caller.
 pcg_status launch_mass_tsc(const int32_t *grid, long long ncells, long long n, const float *const *pos,
                            const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
-                           unsigned *flags, cudaStream_t s);
+                           unsigned *flags, unsigned long long *n_invalid, cudaStream_t s);
 }  // namespace tsc
 namespace mm {
 namespace {
@@ -609,10 +637,12 @@ pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64
     A.n = n;
     A.M = M;
     A.flags = stats ? &stats->error_flags : nullptr;
+    A.n_invalid = stats ? &stats->n_invalid : nullptr;
     cudaStream_t s = as_stream(stream);
     pcg_status st = zero_f32(M, (size_t)ncells * (order == 2 ? 1125 : Win<NC>::NB), s);
     if (st != PCG_OK || n == 0) return st;
-    if (order == 2) return tsc::launch_mass_tsc(grid, ncells, n, pos, w, omega, cell_offsets, M, A.flags, s);
+    if (order == 2)
+        return tsc::launch_mass_tsc(grid, ncells, n, pos, w, omega, cell_offsets, M, A.flags, A.n_invalid, s);
     switch (precision) {
         case 0: return launch<TF32, NC>(A, s);
         case 1: return launch<BF16, NC>(A, s);

@@ -44,6 +44,7 @@ struct Args {
     long long n;
     float *M;
     unsigned *flags;
+    unsigned long long *n_invalid;
 };
 
 
@@ -144,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
     const int tid = threadIdx.x;
     const int a = tid >> 3, h = tid & 7;
     const int ax = a & 3, ay = (a >> 2) & 3, az = a >> 4;
+    unsigned n_inv = 0;
 
     for (long long cell = blockIdx.x; cell < A.ncells; cell += gridDim.x) {
         const int cx = (int)(cell % A.N[0]);
@@ -187,8 +189,12 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
                     for (int c = 0; c < 9; ++c) S[tid][c] = 0.f;
                     const bool ok = x >= 0.f && x < (float)A.N[0] && y >= 0.f && y < (float)A.N[1] && z >= 0.f &&
                                     z < (float)A.N[2];
-                    if (ok) particle_global(A, x, y, z, wq, ox, oy, oz);
-                    if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
+                    if (ok) {
+                        particle_global(A, x, y, z, wq, ox, oy, oz);
+                        if (A.flags) atomicOr(A.flags, PCG_FLAG_CELL_MISMATCH);
+                    } else {
+                        ++n_inv;  // outside the domain or NaN: skipped
+                    }
                 }
             }
             __syncthreads();
@@ -230,6 +236,17 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
         flush_row<0>(A.M, g, ax, ay, az, h, acc);
         flush_row<1>(A.M, g, ax, ay, az, h, acc);
     }
+    // the tail pass: slots [offs[ncells], n) are listed under no cell (the sort's
+    // sentinel bin of invalid particles, or particles appended after the sort)
+    for (long long p = (long long)A.offs[A.ncells] + (long long)blockIdx.x * kThreads + tid; p < A.n;
+         p += (long long)gridDim.x * kThreads) {
+        const float x = A.x[p], y = A.y[p], z = A.z[p];
+        const bool ok = x >= 0.f && x < (float)A.N[0] && y >= 0.f && y < (float)A.N[1] && z >= 0.f &&
+                        z < (float)A.N[2];
+        if (ok) particle_global(A, x, y, z, A.w[p], A.ox[p], A.oy[p], A.oz[p]);
+        else ++n_inv;
+    }
+    warp_add_u64(A.n_invalid, n_inv);
 }
 
 }  // namespace
@@ -237,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
 // M (float[ncells][125][9]) must be zeroed by the caller; grid edges >= 5.
 pcg_status launch_mass_tsc(const int32_t *grid, long long ncells, long long n, const float *const *pos,
                            const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
-                           unsigned *flags, cudaStream_t s) {
+                           unsigned *flags, unsigned long long *n_invalid, cudaStream_t s) {
     Args A{};
     for (int mu = 0; mu < 3; ++mu) A.N[mu] = grid[mu];
     A.ncells = ncells;
@@ -252,6 +269,7 @@ pcg_status launch_mass_tsc(const int32_t *grid, long long ncells, long long n, c
     A.n = n;
     A.M = M;
     A.flags = flags;
+    A.n_invalid = n_invalid;
     const long long cap = num_sms();
     const long long ctas = ncells < cap ? ncells : cap;
     prof::Mark mk("mass_tsc_simt", s);

@@ -55,3 +55,20 @@ def test_roofline_entry_scales_traffic_to_a_full_launch():
     assert e["achieved"] == 1000.0 and e["frac"] == 1.0  # 2 GB in 2 ms against a 1000 GB/s peak
     assert e["traffic"] == 4e8  # captured on 1e6 units, reported for 4e6
     assert bench.roofline_entry("k", prof, 2e9, 1000.0, {}, 4e6)["traffic"] is None
+
+
+def test_all_core_oracle_leg_sums_private_grids():
+    """The all-core CPU leg splits the particles over threads, one private J
+    each: the summed grid equals one call over every particle (up to the order
+    of the fp64 sums)."""
+    import numpy as np
+    import oracle
+    import synth
+    d = synth.cic3d_drift(grid=(16, 16, 16), ppc=4)
+    n = d["n"]
+    ranges = [(0, n // 3), (n // 3, n // 2), (n // 2, n)]
+    J = bench.oracle_on_threads(d, ranges, 3)
+    Jr, _ = oracle.deposit_current(d["grid"], d["order"], d["pos"], d["vel"], d["q"])
+    assert np.abs(J - Jr).max() <= 1e-12 * np.abs(Jr).max()
+    threads, cpu = bench.cpu_threads_for(d)
+    assert 1 <= threads <= cpu["usable"] and cpu["model"]

@@ -187,3 +187,49 @@ def test_tsc_tensor_precisions_are_not_built():
     d = synth.mass3d(grid=(5, 5, 5), ppc=2, seed=4)
     with pytest.raises(pcg.PcgError):
         _assemble_tsc(pcg, d["grid"], d["pos"], d["w"], d["omega"], precision="tf32")
+
+
+@pytest.mark.parametrize("precision,order", [("tf32", 1), ("bf16", 1), ("simt", 1), ("simt", 2)])
+def test_invalid_particles_are_skipped_and_counted(precision, order):
+    # NaN and x = N before the sort (parked in the sentinel bin after the last
+    # cell: the tail pass), and coordinates made invalid after the sort while
+    # still listed under a cell: all are skipped and counted in n_invalid
+    pcg = need_gpu()
+    grid = (6, 6, 6)
+    d = synth.mass3d(grid=grid, ppc=8, seed=5)
+    pos = [p.copy() for p in d["pos"]]
+    rng = np.random.default_rng(7)
+    bad = rng.choice(d["n"], 12, replace=False)
+    pos[0][bad[:6]] = np.nan
+    pos[1][bad[6:]] = np.float32(grid[1])
+    dp = [dev(p) for p in pos]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(d["w"])] + [dev(o) for o in d["omega"]])
+    arrs = [host(t).copy() for t in out]
+    listed = int(host(offs)[-1])
+    assert listed == d["n"] - 12
+    idx = rng.choice(listed, 10, replace=False)
+    arrs[2][idx[:5]] = np.float32(-0.5)
+    arrs[0][idx[5:]] = np.float32(np.inf)
+    stats = pcg.new_stats()
+    M = pcg.assemble_mass_matrix(grid, [dev(a) for a in arrs[:3]], dev(arrs[3]), [dev(a) for a in arrs[4:7]],
+                                 offs, precision=precision, stats=stats, order=order)
+    ref = oracle.mass_matrix if order == 1 else oracle.mass_matrix_tsc
+    Mr, ninv = ref(grid, arrs[:3], arrs[3], arrs[4:7])
+    assert ninv == 22
+    assert stats_dict(stats)["n_invalid"] == 22
+    assert rel_frobenius(host(M), Mr) <= TOL[precision]
+
+
+def test_scalar_invalid_particles_are_skipped_and_counted():
+    pcg = need_gpu()
+    grid = (5, 4, 6)
+    d = synth.mass3d(grid=grid, ppc=9, seed=8)
+    pos = [p.copy() for p in d["pos"]]
+    pos[2][:7] = np.nan
+    dp = [dev(p) for p in pos]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(d["w"])])
+    stats = pcg.new_stats()
+    M = pcg.assemble_mass_matrix_scalar(grid, out[:3], out[3], offs, precision="tf32", stats=stats)
+    Mr, ninv = oracle.mass_matrix_scalar(grid, pos, d["w"])
+    assert ninv == 7 and stats_dict(stats)["n_invalid"] == 7
+    assert rel_frobenius(host(M), Mr) <= MASS_TOL

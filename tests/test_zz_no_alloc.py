@@ -15,6 +15,7 @@ import pytest
 import synth
 from helpers import DEPOSIT_TOL, dev, host, need_gpu
 
+PCG_ERR_INVALID_ARG = 1
 PCG_ERR_WORKSPACE = 2
 
 
@@ -39,6 +40,25 @@ def test_noalloc_rejects_more_chunks_than_its_array_holds():
     st = lib.pcg_deposit_current_noalloc(3, _grid((64, 64, 64)), 1, 8, 2, 0, (1 << 30) + 1, p3, p3, vp, vp,
                                          vp, None, None)
     assert st == PCG_ERR_WORKSPACE
+
+
+def test_noalloc_checks_arguments_before_its_size_limit():
+    from particle_cell_grid_gb300 import _lib, build
+    build.build()
+    lib = _lib.load()
+    vp = ctypes.c_void_p(256)
+    p3 = (ctypes.c_void_p * 3)(256, 256, 256)
+    big = (1 << 30) + 1  # beyond the array's chunk limit
+    # an invalid order, tile size or grid is reported as such, not as a workspace shortfall
+    assert lib.pcg_deposit_current_noalloc(3, _grid((64, 64, 64)), 3, 8, 2, 0, big, p3, p3, vp, vp, vp,
+                                           None, None) == PCG_ERR_INVALID_ARG
+    assert lib.pcg_deposit_current_noalloc(3, _grid((64, 64, 64)), 1, 0, 2, 0, big, p3, p3, vp, vp, vp,
+                                           None, None) == PCG_ERR_INVALID_ARG
+    assert lib.pcg_deposit_current_noalloc(3, _grid((64, 0, 64)), 1, 8, 2, 0, big, p3, p3, vp, vp, vp,
+                                           None, None) == PCG_ERR_INVALID_ARG
+    # an unaligned J as well
+    assert lib.pcg_deposit_current_noalloc(3, _grid((64, 64, 64)), 1, 8, 2, 0, big, p3, p3, vp, vp,
+                                           ctypes.c_void_p(260), None, None) == PCG_ERR_INVALID_ARG
 
 
 @pytest.mark.gpu
