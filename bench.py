@@ -591,7 +591,8 @@ def mass_workload(pcg, steps, warmup, dist, peaks, traffic, edge=64):
 
 
 def tsc_workload(pcg, steps, warmup, dist, peaks, traffic, edge=32):
-    """Second-order (TSC) ECSIM mass matrix on CUDA cores, 125 offsets x 3x3 per node."""
+    """Second-order (TSC) ECSIM mass matrix, 125 offsets x 3x3 per node: tcgen05
+    TF32 and BF16, and the CUDA-core baseline."""
     import torch
     import synth
     d = synth.mass3d(grid=(edge, edge, edge))
@@ -600,14 +601,32 @@ def tsc_workload(pcg, steps, warmup, dist, peaks, traffic, edge=32):
     dp = [dev(p) for p in d["pos"]]
     out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(d["w"])] + [dev(o) for o in d["omega"]])
     M = torch.empty(tuple(reversed(grid)) + (125, 3, 3), dtype=torch.float32, device="cuda")
-    step = lambda: pcg.assemble_mass_matrix(grid, out[:3], out[3], out[4:7], offs, precision="simt", M=M, order=2)
-    step()
-    ms = time_steps(step, steps, warmup, dist, torch.cuda.current_stream(), pcg=pcg)
-    timed = pcg.profile_collect()
-    ent = roofline_entry("mass_tsc_simt", timed, n * 28 + M.numel() * 4, peaks["hbm_gbs"], traffic, n)
-    res = {"workload": f"mass3d TSC {edge}^3 x 64 ppc (125 offsets x 3x3 blocks, CUDA cores)", "particles": n,
-           "ms_per_call": round(ms / steps, 4), "M_particles_per_s": round(n / (ms / steps * 1e-3) / 1e6, 1),
-           "roofline": ent, "useful_tflops": round(n * 27 * 27 * 9 * 2 / (ent["avg_ms"] * 1e-3) / 1e12, 2)}
+    res = {"workload": f"mass3d TSC {edge}^3 x 64 ppc (125 offsets x 3x3 blocks)", "particles": n}
+    useful = n * 27 * 27 * 9 * 2
+    # issued tensor flops: per 64-particle chunk of a cell pair, 4 planes of M=128 x N=160 x K=64
+    ncells = int(np.prod(grid))
+    counts = np.diff(offs.cpu().numpy().astype(np.int64)[:ncells + 1])
+    c2 = np.zeros(((grid[0] + 1) // 2) * 2 * grid[1] * grid[2], np.int64).reshape(grid[2], grid[1], -1)
+    c2[:, :, :grid[0]] = counts.reshape(grid[2], grid[1], grid[0])
+    pairs = c2.reshape(grid[2], grid[1], -1, 2)
+    chunks = int(np.maximum((pairs[..., 0] + 31) // 32, (pairs[..., 1] + 31) // 32).sum())
+    issued = chunks * 4 * 128 * 160 * 64 * 2
+    tf32_peak = peaks["bf16_tflops"] / 2.0   # dense TF32 = half the bf16 rate (nominal 1.1 vs 2.25 PF)
+    for prec in ("tf32", "bf16", "simt"):
+        step = lambda: pcg.assemble_mass_matrix(grid, out[:3], out[3], out[4:7], offs, precision=prec, M=M, order=2)
+        step()
+        ms = time_steps(step, steps, warmup, dist, torch.cuda.current_stream(), pcg=pcg)
+        timed = pcg.profile_collect()
+        ent = roofline_entry(f"mass_tsc_{prec}", timed, n * 28 + M.numel() * 4, peaks["hbm_gbs"], traffic, n)
+        r = {"ms_per_call": round(ms / steps, 4), "kernel_ms": ent["avg_ms"],
+             "M_particles_per_s": round(n / (ms / steps * 1e-3) / 1e6, 1), "roofline": ent,
+             "useful_tflops": round(useful / (ent["avg_ms"] * 1e-3) / 1e12, 2)}
+        if prec != "simt":
+            pk = tf32_peak if prec == "tf32" else peaks["bf16_tflops"]
+            r["issued_tflops"] = round(issued / (ent["avg_ms"] * 1e-3) / 1e12, 2)
+            r["tensor_frac_issued"] = round(issued / (ent["avg_ms"] * 1e-3) / 1e12 / pk, 4)
+            r["tensor_peak_tflops"] = pk
+        res[prec] = r
     del dp, out, offs, M
     torch.cuda.empty_cache()
     return res
@@ -711,6 +730,7 @@ def run_gpu(args):
         del d4
         wl["mass3d_64"] = mass_workload(pcg, ks, kw, dist, peaks, {})
         wl["mass3d_tsc_32"] = tsc_workload(pcg, ks, kw, dist, peaks, {})
+        wl["mass3d_tsc_64"] = tsc_workload(pcg, 3, 3, dist, peaks, {}, edge=64)
         d5 = synth.zigzag3d()
         wl["zigzag3d_256"] = zigzag_workload(pcg, d5, ks, kw, dist, peaks, {})
         del d5

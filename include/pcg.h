@@ -325,8 +325,8 @@ PCG_API pcg_status pcg_deposit_zigzag(const int32_t *grid, int32_t tile, int64_t
  *   order      1 or 2.
  *   precision  0 = TF32 tensor cores (tcgen05.mma kind::tf32, fp32 accumulate
  *              in tensor memory); 1 = BF16 tensor cores (kind::f16); 2 = fp32
- *              CUDA cores (no tensor cores; the A/B baseline).  Order 2 runs on
- *              CUDA cores only: precision 0 or 1 returns PCG_ERR_UNSUPPORTED.
+ *              CUDA cores (no tensor cores; the A/B baseline).  Both orders run
+ *              on all three.
  *   n          number of particles.
  *   pos        HOST array of 3 device float[n]; w device float[n] (q^2/m);
  *   omega      HOST array of 3 device float[n] (omega = beta_s B(x_p) / c).

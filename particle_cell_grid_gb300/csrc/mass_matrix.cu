@@ -44,6 +44,7 @@
 #include "common.cuh"
 #include "mass_common.cuh"
 #include "tcgen05.cuh"
+#include "mass_tsc.cuh"
 
 namespace pcg {
 namespace mm {
@@ -585,12 +586,6 @@ extern "C" pcg_status pcg_assemble_mass_matrix_workspace_size(const int32_t *gri
 }
 
 namespace pcg {
-namespace tsc {
-// mass_tsc.cu: the second-order (TSC) assembly on CUDA cores; M zeroed by the caller.
-pcg_status launch_mass_tsc(const int32_t *grid, long long ncells, long long n, const float *const *pos,
-                           const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
-                           unsigned *flags, unsigned long long *n_invalid, cudaStream_t s);
-}  // namespace tsc
 namespace mm {
 namespace {
 
@@ -608,7 +603,6 @@ pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64
         if (grid[mu] < min_edge || grid[mu] > (1 << 20)) return PCG_ERR_INVALID_ARG;
         ncells *= grid[mu];
     }
-    if (order == 2 && precision != 2) return PCG_ERR_UNSUPPORTED;  // TSC: CUDA cores only
     if (ncells >= (1ll << 31)) return PCG_ERR_INVALID_ARG;
     if (M == nullptr || !aligned16(M) || cell_offsets == nullptr) return PCG_ERR_INVALID_ARG;
     if (n > 0 && (pos == nullptr || w == nullptr || pos[0] == nullptr || pos[1] == nullptr || pos[2] == nullptr))
@@ -641,8 +635,24 @@ pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64
     cudaStream_t s = as_stream(stream);
     pcg_status st = zero_f32(M, (size_t)ncells * (order == 2 ? 1125 : Win<NC>::NB), s);
     if (st != PCG_OK || n == 0) return st;
-    if (order == 2)
-        return tsc::launch_mass_tsc(grid, ncells, n, pos, w, omega, cell_offsets, M, A.flags, A.n_invalid, s);
+    if (order == 2) {
+        tsc::Args T{};
+        for (int mu = 0; mu < 3; ++mu) T.N[mu] = grid[mu];
+        T.ncells = ncells;
+        T.x = A.x;
+        T.y = A.y;
+        T.z = A.z;
+        T.w = A.w;
+        T.ox = A.ox;
+        T.oy = A.oy;
+        T.oz = A.oz;
+        T.offs = cell_offsets;
+        T.n = n;
+        T.M = M;
+        T.flags = A.flags;
+        T.n_invalid = A.n_invalid;
+        return precision == 2 ? tsc::launch_mass_tsc(T, s) : tsc::launch_mass_tsc_tc(T, precision, s);
+    }
     switch (precision) {
         case 0: return launch<TF32, NC>(A, s);
         case 1: return launch<BF16, NC>(A, s);

@@ -25,8 +25,7 @@
 // a scalar head and tail: 9-12 reductions per run instead of 27-36 (32^3 x 64
 // ppc: 6.64 -> 5.80 ms).  The cells are walked in order so that the rows they
 // share stay in L2.
-#include "common.cuh"
-#include "mass_common.cuh"
+#include "mass_tsc.cuh"
 
 namespace pcg {
 namespace tsc {
@@ -36,52 +35,6 @@ constexpr int kThreads = 512;
 constexpr int KB = 64;     // particles per staged batch
 constexpr int NU = 64;     // union nodes (4 x 4 x 4)
 
-struct Args {
-    int N[3];
-    long long ncells;
-    const float *x, *y, *z, *w, *ox, *oy, *oz;
-    const uint32_t *offs;
-    long long n;
-    float *M;
-    unsigned *flags;
-    unsigned long long *n_invalid;
-};
-
-
-// Quadratic B-spline support of one coordinate: first node k - 1 with
-// k = i + (xi >= 1/2), and the weights at k-1, k, k+1 for s = x - k.
-__device__ __forceinline__ int tsc_axis(float x, float (&w)[3]) {
-    const int i = (int)x;  // x >= 0
-    const int k = i + (x - (float)i >= 0.5f ? 1 : 0);
-    const float s = x - (float)k;
-    const float a = 0.5f - s, b = 0.5f + s;
-    w[0] = 0.5f * a * a;
-    w[1] = 0.75f - s * s;
-    w[2] = 0.5f * b * b;
-    return k - 1;
-}
-
-__device__ __forceinline__ int wrapi(int i, int N) { return i >= N ? i - N : (i < 0 ? i + N : i); }
-
-// A particle not inside the cell it is listed under: all 27 x 27 x 9
-// contributions straight to global M.
-__device__ void particle_global(const Args &A, float x, float y, float z, float wq, float ox, float oy, float oz) {
-    float wx[3], wy[3], wz[3], s[9];
-    const int fx = tsc_axis(x, wx), fy = tsc_axis(y, wy), fz = tsc_axis(z, wz);
-    alpha_w(wq, ox, oy, oz, s);
-    for (int a = 0; a < 27; ++a) {
-        const int ax = a % 3, ay = (a / 3) % 3, az = a / 9;
-        const long long g = ((long long)wrapi(fz + az, A.N[2]) * A.N[1] + wrapi(fy + ay, A.N[1])) * A.N[0] +
-                            wrapi(fx + ax, A.N[0]);
-        const float Wa = wx[ax] * wy[ay] * wz[az];
-        for (int b = 0; b < 27; ++b) {
-            const int bx = b % 3, by = (b / 3) % 3, bz = b / 9;
-            const int o = (bz - az + 2) * 25 + (by - ay + 2) * 5 + (bx - ax + 2);
-            const float WW = Wa * wx[bx] * wy[by] * wz[bz];
-            for (int c = 0; c < 9; ++c) red_add_f32(A.M + (g * 125 + o) * 9 + c, s[c] * WW);
-        }
-    }
-}
 
 // One run of the flush: the partners bx = LO .. LO + L/9 - 1 of one row, i.e.
 // L consecutive floats of M starting at dst (= (g*125 + o)*9 floats into the
@@ -236,42 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
         flush_row<0>(A.M, g, ax, ay, az, h, acc);
         flush_row<1>(A.M, g, ax, ay, az, h, acc);
     }
-    // the tail pass: slots [offs[ncells], n) are listed under no cell (the sort's
-    // sentinel bin of invalid particles, or particles appended after the sort)
-    for (long long p = (long long)A.offs[A.ncells] + (long long)blockIdx.x * kThreads + tid; p < A.n;
-         p += (long long)gridDim.x * kThreads) {
-        const float x = A.x[p], y = A.y[p], z = A.z[p];
-        const bool ok = x >= 0.f && x < (float)A.N[0] && y >= 0.f && y < (float)A.N[1] && z >= 0.f &&
-                        z < (float)A.N[2];
-        if (ok) particle_global(A, x, y, z, A.w[p], A.ox[p], A.oy[p], A.oz[p]);
-        else ++n_inv;
-    }
+    tail_pass(A, n_inv);
     warp_add_u64(A.n_invalid, n_inv);
 }
 
 }  // namespace
 
-// M (float[ncells][125][9]) must be zeroed by the caller; grid edges >= 5.
-pcg_status launch_mass_tsc(const int32_t *grid, long long ncells, long long n, const float *const *pos,
-                           const float *w, const float *const *omega, const uint32_t *cell_offsets, float *M,
-                           unsigned *flags, unsigned long long *n_invalid, cudaStream_t s) {
-    Args A{};
-    for (int mu = 0; mu < 3; ++mu) A.N[mu] = grid[mu];
-    A.ncells = ncells;
-    A.x = pos[0];
-    A.y = pos[1];
-    A.z = pos[2];
-    A.w = w;
-    A.ox = omega[0];
-    A.oy = omega[1];
-    A.oz = omega[2];
-    A.offs = cell_offsets;
-    A.n = n;
-    A.M = M;
-    A.flags = flags;
-    A.n_invalid = n_invalid;
+pcg_status launch_mass_tsc(const Args &A, cudaStream_t s) {
     const long long cap = num_sms();
-    const long long ctas = ncells < cap ? ncells : cap;
+    const long long ctas = A.ncells < cap ? A.ncells : cap;
     prof::Mark mk("mass_tsc_simt", s);
     mass_tsc_kernel<<<(unsigned)ctas, kThreads, 0, s>>>(A);
     return launch_status();

@@ -121,6 +121,27 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Warp-collective load of 8 consecutive 32-bit TMEM columns without waiting;
+// the registers are valid only after tmem_wait_ld(...) on them.
+__device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t *r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Wait for this thread's outstanding tcgen05.ld, then pin every register of `r`
+// behind the wait (an empty volatile asm per register), so that no use of a
+// loaded value is scheduled before the data has arrived.
+template <int NR>
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[NR]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < NR; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // ---- bulk asynchronous copies (TMA engine, no tensor map) ------------------
 // dst[0..bytes) += src[0..bytes) element-wise in fp32, global <- shared; both
 // addresses 16-byte aligned, bytes a multiple of 16.  Completion is tracked by

@@ -151,7 +151,8 @@ def test_mass_matrix_rejects_bad_arguments(lib):
         grid, order, prec, 10, ptrs, vp, ptrs, vp, M, None, None, 0, None)
     assert call(grid=_grid(2, 8, 8)) == 1                    # 27 offsets need an edge >= 3
     assert call(order=3) == 1
-    assert call(order=2) == 3                                # TSC is built on CUDA cores only
+    assert call(grid=_grid(8, 4, 8), order=2) == 1           # 125 offsets need an edge >= 5
+    assert call(grid=_grid(5, 5, 5), order=2, prec=3) == 1
     assert call(prec=3) == 1
     assert call(M=ctypes.c_void_p(260)) == 1
 
@@ -169,10 +170,11 @@ def test_scalar_mass_rejects_bad_arguments(lib):
     assert f(g, 1, 0, 10, arr, vp, vp, ctypes.c_void_p(4100), None, None) == 1  # M unaligned
 
 
-def test_tsc_mass_rejects_small_grids_and_tensor_precisions(lib):
+def test_tsc_mass_rejects_small_grids_and_bad_precisions(lib):
     vp = ctypes.c_void_p(4096)
     arr = (ctypes.c_void_p * 3)(4096, 4096, 4096)
     f = lib.pcg_assemble_mass_matrix
     assert f(_grid(8, 4, 8), 2, 2, 10, arr, vp, arr, vp, vp, None, None, 0, None) == 1  # order 2 needs >= 5
     assert f(_grid(8, 8, 8), 3, 2, 10, arr, vp, arr, vp, vp, None, None, 0, None) == 1  # order 3
-    assert f(_grid(8, 8, 8), 2, 0, 10, arr, vp, arr, vp, vp, None, None, 0, None) == 3  # TSC on tensor cores
+    assert f(_grid(8, 8, 8), 2, -1, 10, arr, vp, arr, vp, vp, None, None, 0, None) == 1  # precision
+    assert f(_grid(8, 8, 8), 2, 0, 10, arr, vp, arr, vp, ctypes.c_void_p(4100), None, None, 0, None) == 1  # M align

@@ -120,6 +120,33 @@ def test_mass3d_64():
             assert rel_frobenius(M[box], Mr[box]) <= MASS_TOL, (precision, lo)
 
 
+def test_mass3d_tsc_64():
+    """Second-order (TSC) mass matrix at 64^3 x 64 ppc on tcgen05 (TF32, BF16):
+    sampled node boxes against the oracle fed every particle that can reach them."""
+    pcg = need_gpu()
+    d = synth.mass3d()
+    grid = d["grid"]
+    dp = [dev(p) for p in d["pos"]]
+    out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(d["w"])] + [dev(o) for o in d["omega"]])
+    del dp
+    refs = []
+    for lo, hi in [((0, 0, 0), (5, 5, 5)), ((30, 41, 59), (36, 46, 64))]:
+        idx = _near_box(d["pos"], grid, lo, hi, margin=3)
+        Mr, _ = oracle.mass_matrix_tsc(grid, [p[idx] for p in d["pos"]], d["w"][idx], [o[idx] for o in d["omega"]])
+        box = _box_index(grid, lo, hi)
+        refs.append((box, Mr[box].copy()))
+        del Mr
+    for precision in ("tf32", "bf16"):
+        stats = pcg.new_stats()
+        M = host(pcg.assemble_mass_matrix(grid, out[:3], out[3], out[4:7], offs, precision=precision,
+                                          stats=stats, order=2))
+        st = stats_dict(stats)
+        assert st["error_flags"] == 0 and st["n_invalid"] == 0
+        for box, Mb in refs:
+            assert rel_frobenius(M[box], Mb) <= MASS_TOL, precision
+        del M
+
+
 def test_cic1d_grad_ten_million():
     """The gradient at N = 10^7 (the size the pages time it at), checked whole."""
     pcg = need_gpu()

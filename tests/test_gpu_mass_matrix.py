@@ -142,19 +142,22 @@ def _assemble_tsc(pcg, grid, pos, w, omega, precision="simt", stats=None):
                                     order=2)
 
 
-@pytest.mark.parametrize("grid,ppc", [((5, 6, 5), 20), ((8, 8, 8), 64), ((7, 5, 9), 3)])
-def test_tsc_matches_oracle(grid, ppc):
+@pytest.mark.parametrize("precision", ["tf32", "bf16", "simt"])
+@pytest.mark.parametrize("grid,ppc", [((5, 6, 5), 20), ((8, 8, 8), 64), ((7, 5, 9), 3), ((9, 6, 5), 130)])
+def test_tsc_matches_oracle(grid, ppc, precision):
     pcg = need_gpu()
     d = synth.mass3d(grid=grid, ppc=ppc, seed=sum(grid) + ppc + 7)
     stats = pcg.new_stats()
-    M = host(_assemble_tsc(pcg, grid, d["pos"], d["w"], d["omega"], stats=stats))
+    M = host(_assemble_tsc(pcg, grid, d["pos"], d["w"], d["omega"], stats=stats, precision=precision))
     Mr, _ = oracle.mass_matrix_tsc(grid, d["pos"], d["w"], d["omega"])
     assert M.shape == Mr.shape
-    assert rel_frobenius(M, Mr) <= 1e-5
-    assert stats_dict(stats)["error_flags"] == 0
+    assert rel_frobenius(M, Mr) <= TOL[precision]
+    st = stats_dict(stats)
+    assert st["error_flags"] == 0 and st["n_invalid"] == 0
 
 
-def test_tsc_variable_occupancy_and_mismatch():
+@pytest.mark.parametrize("precision", ["tf32", "bf16", "simt"])
+def test_tsc_variable_occupancy_and_mismatch(precision):
     pcg = need_gpu()
     grid = (6, 7, 5)
     rng = np.random.default_rng(12)
@@ -169,7 +172,7 @@ def test_tsc_variable_occupancy_and_mismatch():
     w = rng.uniform(0.5, 1.5, n).astype(np.float32)
     omega = [rng.normal(0, 0.8, n).astype(np.float32) for _ in range(3)]
     Mr, _ = oracle.mass_matrix_tsc(grid, pos, w, omega)
-    assert rel_frobenius(host(_assemble_tsc(pcg, grid, pos, w, omega)), Mr) <= 1e-5
+    assert rel_frobenius(host(_assemble_tsc(pcg, grid, pos, w, omega, precision=precision)), Mr) <= TOL[precision]
     # arrays that no longer match their cell layout: exact through the slow path, flagged
     dp = [dev(p) for p in pos]
     out, offs = pcg.tile_sort(grid, 1, dp, dp + [dev(w)] + [dev(o) for o in omega])
@@ -177,19 +180,13 @@ def test_tsc_variable_occupancy_and_mismatch():
     arrs = [host(t)[perm2] for t in out]
     stats = pcg.new_stats()
     M = pcg.assemble_mass_matrix(grid, [dev(a) for a in arrs[:3]], dev(arrs[3]), [dev(a) for a in arrs[4:7]], offs,
-                                 precision="simt", stats=stats, order=2)
-    assert rel_frobenius(host(M), Mr) <= 1e-5
+                                 precision=precision, stats=stats, order=2)
+    assert rel_frobenius(host(M), Mr) <= TOL[precision]
     assert stats_dict(stats)["error_flags"] & 2
 
 
-def test_tsc_tensor_precisions_are_not_built():
-    pcg = need_gpu()
-    d = synth.mass3d(grid=(5, 5, 5), ppc=2, seed=4)
-    with pytest.raises(pcg.PcgError):
-        _assemble_tsc(pcg, d["grid"], d["pos"], d["w"], d["omega"], precision="tf32")
-
-
-@pytest.mark.parametrize("precision,order", [("tf32", 1), ("bf16", 1), ("simt", 1), ("simt", 2)])
+@pytest.mark.parametrize("precision,order", [("tf32", 1), ("bf16", 1), ("simt", 1), ("tf32", 2), ("bf16", 2),
+                                             ("simt", 2)])
 def test_invalid_particles_are_skipped_and_counted(precision, order):
     # NaN and x = N before the sort (parked in the sentinel bin after the last
     # cell: the tail pass), and coordinates made invalid after the sort while
