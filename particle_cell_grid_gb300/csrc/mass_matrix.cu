@@ -651,7 +651,8 @@ pcg_status assemble(const int32_t *grid, int32_t order, int32_t precision, int64
         T.M = M;
         T.flags = A.flags;
         T.n_invalid = A.n_invalid;
-        return precision == 2 ? tsc::launch_mass_tsc(T, s) : tsc::launch_mass_tsc_tc(T, precision, s);
+        st = precision == 2 ? tsc::launch_mass_tsc(T, s) : tsc::launch_mass_tsc_tc(T, precision, s);
+        return st == PCG_OK ? tsc::launch_mass_tsc_mirror(T, s) : st;
     }
     switch (precision) {
         case 0: return launch<TF32, NC>(A, s);

@@ -12,19 +12,20 @@
 //                 outside each particle's own 27, is what this kernel does.
 //   Sec. 3.4:     displacements in {-2..2}^3: 125 offsets per node, all kept.
 //
-// GB300 design (first version, CUDA cores).  One 512-thread CTA per cell: the
-// union of the supports of the cell's particles is the 4x4x4 node block
-// starting one node below the cell.  Thread (a, h) owns union node a (0..63)
-// and the 8 partner nodes b = 8h..8h+7, i.e. 72 accumulators (8 pairs x 9
-// components) in registers, for every particle of the cell.  Particles are
-// staged 64 at a time: their per-node weights (64 x 64 floats, zero outside
-// their 27 nodes) and coefficients w alpha in shared memory.  At the end of the
-// cell every pair within +-2 nodes per axis is added to M: each thread's 4
-// partners along x are 4 consecutive offsets, i.e. a run of up to 36
-// consecutive floats of M, which goes out as 16-byte vector reductions between
-// a scalar head and tail: 9-12 reductions per run instead of 27-36 (32^3 x 64
-// ppc: 6.64 -> 5.80 ms).  The cells are walked in order so that the rows they
-// share stay in L2.
+// GB300 design (CUDA cores; the A/B baseline of the tcgen05 kernel in
+// mass_tsc_tc.cu).  One 512-thread CTA per cell: the union of the supports of
+// the cell's particles is the 4x4x4 node block starting one node below the
+// cell.  Thread (a, h) owns union node a (0..63) and the 8 partner nodes
+// b = 8h..8h+7, i.e. 72 accumulators (8 pairs x 9 components) in registers, for
+// every particle of the cell.  Particles are staged 64 at a time: their
+// per-node weights (64 x 64 floats, zero outside their 27 nodes) and
+// coefficients w alpha in shared memory.  At the end of the cell the pairs in
+// the stored half of M (displacement >= 0; the mirror half is copied by
+// mirror_kernel afterwards) are added to M: each thread's 4 partners along x
+// are consecutive offsets, one run of up to 36 consecutive floats of M, which
+// goes out through the thread's shared-memory slot as aligned 16-byte vector
+// reductions (flush_slot: the same loop in every lane).  The cells are walked
+// in order so that the rows they share stay in L2.
 #include "mass_tsc.cuh"
 
 namespace pcg {
@@ -36,56 +37,32 @@ constexpr int KB = 64;     // particles per staged batch
 constexpr int NU = 64;     // union nodes (4 x 4 x 4)
 
 
-// One run of the flush: the partners bx = LO .. LO + L/9 - 1 of one row, i.e.
-// L consecutive floats of M starting at dst (= (g*125 + o)*9 floats into the
-// 16-byte-aligned M).  HEAD = floats up to the next 16-byte boundary: scalar
-// reductions for the head and the tail, 16-byte vector reductions between, so
-// every vector address is 16-byte aligned.  All-zero quads are skipped.
-template <int ROW, int LO, int L, int HEAD>
-__device__ __forceinline__ void flush_run(float *dst, const float (&acc)[8][9]) {
-#define PCG_TSC_V(e) acc[4 * ROW + LO + (e) / 9][(e) % 9]
-#pragma unroll
-    for (int e = 0; e < HEAD && e < L; ++e)
-        if (PCG_TSC_V(e) != 0.f) red_add_f32(dst + e, PCG_TSC_V(e));
-#pragma unroll
-    for (int e = HEAD; e + 4 <= L; e += 4) {
-        const float v0 = PCG_TSC_V(e), v1 = PCG_TSC_V(e + 1), v2 = PCG_TSC_V(e + 2), v3 = PCG_TSC_V(e + 3);
-        if (v0 != 0.f || v1 != 0.f || v2 != 0.f || v3 != 0.f) red_add_v4_f32(dst + e, v0, v1, v2, v3);
-    }
-#pragma unroll
-    for (int e = HEAD + (L - HEAD) / 4 * 4; e < L; ++e)
-        if (e >= HEAD && PCG_TSC_V(e) != 0.f) red_add_f32(dst + e, PCG_TSC_V(e));
-#undef PCG_TSC_V
+// Row ROW (partners 4 ROW .. 4 ROW + 3 of this thread, one x-row of the union)
+// of node (ax, ay, az): its stored part (offsets >= 62) as one run of M,
+// flushed through the thread's slot.
+template <int ROW>
+__device__ __forceinline__ void flush_row(float *M, long long total, float *slot, long long g, int ax, int ay,
+                                          int az, int h, const float (&acc)[8][9]) {
+    const int b0 = 8 * h + 4 * ROW;
+    Run r{0, 0, 0};
+    const bool act = stored_run(ax, ((b0 >> 2) & 3) - ay, (b0 >> 4) - az, r);
+    flush_slot(M, total, slot, (g * 125 + r.o0) * 9, 9 * r.lo, 9 * r.cnt, act,
+               [&](int k) { return acc[4 * ROW + k / 9][k % 9]; });
 }
 
-// Row ROW (partners 4 ROW .. 4 ROW + 3 of this thread, one x-row of the union)
-// of node (ax, ay, az) into M: the partners within +-2 along x are bx = 0..2
-// (ax = 0), 1..3 (ax = 3) or 0..3.
-template <int ROW>
-__device__ __forceinline__ void flush_row(float *M, long long g, int ax, int ay, int az, int h,
-                                          const float (&acc)[8][9]) {
-    const int b0 = 8 * h + 4 * ROW;
-    const int dy = ((b0 >> 2) & 3) - ay, dz = (b0 >> 4) - az;
-    if (dy < -2 || dy > 2 || dz < -2 || dz > 2) return;
-    const int lo = ax == 3 ? 1 : 0;
-    const int o = (dz + 2) * 25 + (dy + 2) * 5 + (lo - ax + 2);
-    const long long start = (g * 125 + o) * 9;
-    const int head = (int)((4 - (start & 3)) & 3);
-    float *dst = M + start;
-    const int kind = ax == 0 ? 1 : (ax == 3 ? 2 : 0);  // 0: 4 partners from bx 0; 1: 3 from 0; 2: 3 from 1
-    switch (kind * 4 + head) {
-        case 0: flush_run<ROW, 0, 36, 0>(dst, acc); break;
-        case 1: flush_run<ROW, 0, 36, 1>(dst, acc); break;
-        case 2: flush_run<ROW, 0, 36, 2>(dst, acc); break;
-        case 3: flush_run<ROW, 0, 36, 3>(dst, acc); break;
-        case 4: flush_run<ROW, 0, 27, 0>(dst, acc); break;
-        case 5: flush_run<ROW, 0, 27, 1>(dst, acc); break;
-        case 6: flush_run<ROW, 0, 27, 2>(dst, acc); break;
-        case 7: flush_run<ROW, 0, 27, 3>(dst, acc); break;
-        case 8: flush_run<ROW, 1, 27, 0>(dst, acc); break;
-        case 9: flush_run<ROW, 1, 27, 1>(dst, acc); break;
-        case 10: flush_run<ROW, 1, 27, 2>(dst, acc); break;
-        default: flush_run<ROW, 1, 27, 3>(dst, acc); break;
+// The mirror half: M[g][o] = M[g + d(o)][124 - o] for every offset o < 62,
+// a streaming copy within M (reads the stored half, writes the other).
+__global__ void mirror_kernel(float *__restrict__ M, int Nx, int Ny, int Nz, long long ncells) {
+    const long long total = ncells * (kMidOffset * 9);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long g = i / (kMidOffset * 9);
+        const int r = (int)(i - g * (kMidOffset * 9));
+        const int o = r / 9, c = r - 9 * (r / 9);
+        const int dx = o % 5 - 2, dy = (o / 5) % 5 - 2, dz = o / 25 - 2;
+        const int gx = (int)(g % Nx), gy = (int)((g / Nx) % Ny), gz = (int)(g / ((long long)Nx * Ny));
+        const long long gp = ((long long)wrapi(gz + dz, Nz) * Ny + wrapi(gy + dy, Ny)) * Nx + wrapi(gx + dx, Nx);
+        M[(g * 125 + o) * 9 + c] = M[(gp * 125 + (124 - o)) * 9 + c];
     }
 }
 
@@ -94,6 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
     __shared__ float S[KB][9];        // w alpha
     __shared__ int rel[KB][3];        // first node relative to the union, -1 = skip
     __shared__ float wax[KB][3][3];   // per-axis weights
+    extern __shared__ __align__(16) float slots[];  // kSlot floats per thread, for the flush
+    float *slot = slots + kSlot * threadIdx.x;
 
     const int tid = threadIdx.x;
     const int a = tid >> 3, h = tid & 7;
@@ -186,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
         // ---- flush the pairs within +-2 nodes per axis: two x-rows per thread ----
         const long long g = ((long long)wrapi(cz - 1 + az, A.N[2]) * A.N[1] + wrapi(cy - 1 + ay, A.N[1])) * A.N[0] +
                             wrapi(cx - 1 + ax, A.N[0]);
-        flush_row<0>(A.M, g, ax, ay, az, h, acc);
-        flush_row<1>(A.M, g, ax, ay, az, h, acc);
+        flush_row<0>(A.M, A.ncells * 1125, slot, g, ax, ay, az, h, acc);
+        flush_row<1>(A.M, A.ncells * 1125, slot, g, ax, ay, az, h, acc);
     }
     tail_pass(A, n_inv);
     warp_add_u64(A.n_invalid, n_inv);
@@ -195,11 +174,23 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_kernel(Args A) {
 
 }  // namespace
 
+pcg_status launch_mass_tsc_mirror(const Args &A, cudaStream_t s) {
+    const long long total = A.ncells * (kMidOffset * 9);
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    prof::Mark mk("mass_tsc_mirror", s);
+    mirror_kernel<<<(unsigned)blocks, 256, 0, s>>>(A.M, A.N[0], A.N[1], A.N[2], A.ncells);
+    return launch_status();
+}
+
 pcg_status launch_mass_tsc(const Args &A, cudaStream_t s) {
     const long long cap = num_sms();
     const long long ctas = A.ncells < cap ? A.ncells : cap;
     prof::Mark mk("mass_tsc_simt", s);
-    mass_tsc_kernel<<<(unsigned)ctas, kThreads, 0, s>>>(A);
+    constexpr int kSlotBytes = kSlot * 4 * kThreads;
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(mass_tsc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSlotBytes));
+    mass_tsc_kernel<<<(unsigned)ctas, kThreads, kSlotBytes, s>>>(A);
     return launch_status();
 }
 

@@ -65,7 +65,8 @@ struct Lay {
     static constexpr int KSTEPS = KC * EB / 32;               // 32 bytes of K per instruction
     // one CTA per SM: the CTA takes all 512 tensor-memory columns, so shared
     // memory is sized to leave no room for a second CTA
-    static constexpr int SMEM = (2 * STAGE + 1024 > 120 * 1024) ? 2 * STAGE + 1024 : 120 * 1024;
+    static constexpr int USED = 2 * STAGE + kSlot * 4 * kThreads + 64;
+    static constexpr int SMEM = USED > 120 * 1024 ? USED : 120 * 1024;
 };
 
 // Byte offset of (row r, K column kk) inside an operand of K-atoms of `atom`
@@ -81,53 +82,6 @@ template <int MODE>
 __device__ __forceinline__ void put(unsigned char *p, float v) {
     if (MODE == TF32) *reinterpret_cast<uint32_t *>(p) = tc::to_tf32(v);
     else *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
-}
-
-// One run of L consecutive floats of M starting at dst (16-byte-aligned M, HEAD
-// floats up to the next 16-byte boundary): scalar head and tail, 16-byte
-// vector reductions between; all-zero quads skipped.  v[LO*9 ..] are the run's
-// values (partners bx = LO .. LO + L/9 - 1, nine components each).
-template <int LO, int L, int HEAD>
-__device__ __forceinline__ void flush_run(float *dst, const uint32_t (&v)[NROW]) {
-#define PCG_TSC_V(e) __uint_as_float(v[LO * 9 + (e)])
-#pragma unroll
-    for (int e = 0; e < HEAD && e < L; ++e)
-        if (PCG_TSC_V(e) != 0.f) red_add_f32(dst + e, PCG_TSC_V(e));
-#pragma unroll
-    for (int e = HEAD; e + 4 <= L; e += 4) {
-        const float v0 = PCG_TSC_V(e), v1 = PCG_TSC_V(e + 1), v2 = PCG_TSC_V(e + 2), v3 = PCG_TSC_V(e + 3);
-        if (v0 != 0.f || v1 != 0.f || v2 != 0.f || v3 != 0.f) red_add_v4_f32(dst + e, v0, v1, v2, v3);
-    }
-#pragma unroll
-    for (int e = HEAD + (L - HEAD) / 4 * 4; e < L; ++e)
-        if (e >= HEAD && PCG_TSC_V(e) != 0.f) red_add_f32(dst + e, PCG_TSC_V(e));
-#undef PCG_TSC_V
-}
-
-// The by-row of node (ax, ay, az) of a union: partners bx with |bx - ax| <= 2
-// (bx 0..2 when ax = 0, 1..3 when ax = 3, else 0..3), as one run of M.
-__device__ __forceinline__ void flush_row(float *M, long long g, int ax, int dy, int dz,
-                                          const uint32_t (&v)[NROW]) {
-    const int lo = ax == 3 ? 1 : 0;
-    const int o = (dz + 2) * 25 + (dy + 2) * 5 + (lo - ax + 2);
-    const long long start = (g * 125 + o) * 9;
-    const int head = (int)((4 - (start & 3)) & 3);
-    float *dst = M + start;
-    const int kind = ax == 0 ? 1 : (ax == 3 ? 2 : 0);  // 0: 4 partners from bx 0; 1: 3 from 0; 2: 3 from 1
-    switch (kind * 4 + head) {
-        case 0: flush_run<0, 36, 0>(dst, v); break;
-        case 1: flush_run<0, 36, 1>(dst, v); break;
-        case 2: flush_run<0, 36, 2>(dst, v); break;
-        case 3: flush_run<0, 36, 3>(dst, v); break;
-        case 4: flush_run<0, 27, 0>(dst, v); break;
-        case 5: flush_run<0, 27, 1>(dst, v); break;
-        case 6: flush_run<0, 27, 2>(dst, v); break;
-        case 7: flush_run<0, 27, 3>(dst, v); break;
-        case 8: flush_run<1, 27, 0>(dst, v); break;
-        case 9: flush_run<1, 27, 1>(dst, v); break;
-        case 10: flush_run<1, 27, 2>(dst, v); break;
-        default: flush_run<1, 27, 3>(dst, v); break;
-    }
 }
 
 // Per-axis weights of a coordinate over the 4 union nodes u = 0..3 of its cell
@@ -252,20 +206,22 @@ __device__ __forceinline__ void issue(uint32_t tmem, uint32_t dcol, const unsign
     }
 }
 
-// Read one plane's accumulator back and add it to M.  Warp w reads lane
-// quadrant w & 3 (rows 32 (w & 3) .. +31: cell j = row / 64, union node
-// a = row % 64) and by-rows 2 (w >> 2), 2 (w >> 2) + 1.
-__device__ __forceinline__ void drain(const Args &A, const Pair &pr, int p, uint32_t tmem, uint32_t dcol) {
+// Read one plane's accumulator back and add its stored half to M.  Warp w reads
+// lane quadrant w & 3 (rows 32 (w & 3) .. +31: cell j = row / 64, union node
+// a = row % 64) and by-rows 2 (w >> 2), 2 (w >> 2) + 1; each row of a node is
+// one run of M, flushed through the lane's slot.
+__device__ __forceinline__ void drain(const Args &A, const Pair &pr, int p, uint32_t tmem, uint32_t dcol,
+                                      float *slot) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = 32 * (warp & 3) + lane;
     const int j = row >> 6, a = row & 63;
     if (pr.n[j] == 0) return;  // warp-uniform: a warp's rows belong to one cell
     const int ax = a & 3, ay = (a >> 2) & 3, az = a >> 4;
-    const int dz = p - az;
     const int gx = wrapi(pr.cx0 + j - 1 + ax, A.N[0]);
     const int gy = wrapi(pr.cy - 1 + ay, A.N[1]);
     const int gz = wrapi(pr.cz - 1 + az, A.N[2]);
     const long long g = ((long long)gz * A.N[1] + gy) * A.N[0] + gx;
+    const long long total = A.ncells * 1125;
     const uint32_t lanebase = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + dcol;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -274,8 +230,10 @@ __device__ __forceinline__ void drain(const Args &A, const Pair &pr, int p, uint
 #pragma unroll
         for (int m = 0; m < NROW / 8; ++m) tc::tmem_ld8_async(lanebase + NROW * by + 8 * m, v + 8 * m);
         tc::tmem_wait_ld(v);
-        const int dy = by - ay;
-        if (dy >= -2 && dy <= 2 && dz >= -2 && dz <= 2) flush_row(A.M, g, ax, dy, dz, v);
+        Run r{0, 0, 0};
+        const bool act = stored_run(ax, by - ay, p - az, r);
+        flush_slot(A.M, total, slot, (g * 125 + r.o0) * 9, 9 * r.lo, 9 * r.cnt, act,
+                   [&](int k) { return __uint_as_float(v[k]); });
     }
 }
 
@@ -284,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_tc_kernel(Args A) {
     using L = Lay<MODE>;
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char *const stg0 = smem, *const stg1 = smem + L::STAGE;
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + 2 * L::STAGE);  // [0, 1] staging, [2, 3] planes
+    float *slots = reinterpret_cast<float *>(smem + 2 * L::STAGE);       // kSlot floats per thread
+    uint64_t *bar = reinterpret_cast<uint64_t *>(slots + kSlot * kThreads);  // [0, 1] staging, [2, 3] planes
     uint32_t *tslot = reinterpret_cast<uint32_t *>(bar + 4);
     const int tid = threadIdx.x, warp = tid >> 5;
 
@@ -315,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) mass_tsc_tc_kernel(Args A) {
         }
         tph[pend_tb] ^= 1u;
         tc::fence_after_sync();
-        drain(A, pend, pend_p, tmem, 256u * pend_tb);
+        drain(A, pend, pend_p, tmem, 256u * pend_tb, slots + kSlot * threadIdx.x);
         tc::fence_before_sync();
         pend_p = -1;
     };
