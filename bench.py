@@ -78,7 +78,8 @@ KERNEL_SOURCES = {
     "sort": ["tile_sort.cu"] + _COMMON,
     "deposit_tiled": ["deposit_tiled.cuh", "deposit.cuh", "deposit_2d.cu", "deposit_3d.cu"] + _COMMON,
     "deposit_zigzag": ["deposit_zigzag.cu", "deposit_tiled.cuh", "deposit.cuh"] + _COMMON,
-    "mass": ["mass_matrix.cu", "mass_tsc.cu", "mass_common.cuh", "tcgen05.cuh"] + _COMMON,
+    "mass": ["mass_matrix.cu", "mass_cic.cuh", "mass_cic_tc.cu", "mass_tsc.cu", "mass_tsc.cuh", "mass_tsc_tc.cu",
+             "mass_common.cuh", "tcgen05.cuh"] + _COMMON,
     "cic1d": ["cic1d.cu"] + _COMMON,
 }
 

@@ -132,6 +132,14 @@ __device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t *r) {
         : "memory");
 }
 
+// Warp-collective load of 4 consecutive 32-bit TMEM columns without waiting.
+__device__ __forceinline__ void tmem_ld4_async(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
 // Wait for this thread's outstanding tcgen05.ld, then pin every register of `r`
 // behind the wait (an empty volatile asm per register), so that no use of a
 // loaded value is scheduled before the data has arrived.
@@ -170,6 +178,11 @@ __device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count) {
                  : "memory");
 }
 
+// Arrive once on `mbar` (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t *mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(mbar)) : "memory");
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // `max_polls` polls and returns false (the caller records a timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, uint32_t max_polls) {
@@ -182,6 +195,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, uint3
             "selp.b32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
             : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// As mbar_wait, but each poll lets the hardware suspend the thread for up to
+// `hint_ns` nanoseconds until the phase completes, instead of spinning: waiting
+// warps then take no issue slots from the warps doing work.  Gives up after
+// `max_polls` polls (a bound of at most max_polls * hint_ns).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *mbar, uint32_t parity, uint32_t max_polls,
+                                                uint32_t hint_ns) {
+    const uint32_t a = smem_addr(mbar);
+    for (uint32_t i = 0; i < max_polls; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.b32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(a), "r"(parity), "r"(hint_ns)
             : "memory");
         if (done) return true;
     }
