@@ -494,8 +494,11 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
 // consecutive 8-byte words (conflict-free).  With 8 particles per cell per
 // round on average, a warp's longest cell list is ~1.5x the mean (a round of
 // 1024 would leave two thirds of the lanes idle).  A cell holds up to CAP
-// particles per round; further ones, and particles that drifted into the halo,
-// go to a short list deposited with per-particle shared reductions.
+// particles per round.  Particles the fast path does not take (drifted into the
+// halo, beyond CAP in their cell, escaping, invalid) are queued per warp in
+// shared memory (ballot-compacted) and taken by the warp one per lane after its
+// 8 particles: their general path and global reductions then run once per warp
+// instead of inside the unrolled loop whenever any lane of the warp needs it.
 // The next round's particles are loaded into registers before this round is
 // accumulated, so their latency hides behind the accumulation.
 // ---------------------------------------------------------------------------
@@ -505,12 +508,12 @@ struct Cic5Cfg {
     static constexpr int PPT = 8;               // particles per thread per round
     static constexpr int R = THREADS * PPT;     // round size
     static constexpr int CAP = 12;              // staged particles per cell and round
-    static constexpr int HCAP = 512;            // listed halo / overflow particles per round
+    static constexpr int QCAP = PPT * 32;       // queued particles per warp and round: room for all
     using C = TileCfg<3, 1, 8, HALO>;
     static constexpr int NK = C::NKEYS;         // cells of the tile (one thread each)
     static_assert(NK <= THREADS, "one thread per grouped cell");
     static_assert(24 <= 6 * CAP, "the corner values fit in the staging array");
-    static constexpr size_t SMEM = (size_t)3 * CAP * NK * 8 + (size_t)7 * HCAP * 4 + (size_t)NK * 4;
+    static constexpr size_t SMEM = (size_t)3 * CAP * NK * 8 + (size_t)(THREADS / 32) * QCAP * 4 + (size_t)NK * 4;
 };
 
 // Position of a CTA in its work: chunk, tile segment (tile t, valid particles
@@ -593,17 +596,51 @@ __device__ __forceinline__ void stencil_to_global(const Geom &g, float *__restri
         }
 }
 
-// Rare paths of the placing loop, kept out of line: inlined into each of its 8
-// unrolled iterations they multiply the loop's code size.
+// The escape of a particle whose stencil leaves the window, kept out of line.
 static __device__ __noinline__ void escape_to_global(const Geom g, float *J, float x, float y, float z, float qvx,
                                               float qvy, float qvz) {
     deposit_global<3, 1>(g, J, x, y, z, qvx, qvy, qvz);
 }
+// The general path of one particle of tile (ox, oy, oz) that the fast path did
+// not take: 1 invalid (skipped), 2 escaped to J, 0 placed in its own cell (rank
+// below CAP) or deposited straight to J (halo, or beyond CAP).  It runs for a
+// few percent of the particles, from a warp's queue, outside the unrolled loop.
 template <int HALO>
-__device__ __noinline__ void list_full_to_global(const Geom g, float *J, int ox, int oy, int oz, int lx, int ly,
-                                                 int lz, float tx, float ty, float tz, float qvx, float qvy,
-                                                 float qvz) {
-    stencil_to_global<HALO>(g, J, ox, oy, oz, lx, ly, lz, tx, ty, tz, qvx, qvy, qvz);
+__device__ __forceinline__ int slow_particle(const Geom &g, float *J, float2 *st, unsigned *cnt, int ox, int oy,
+                                          int oz, float x, float y, float z, float qvx, float qvy, float qvz) {
+    using C = typename Cic5Cfg<HALO>::C;
+    constexpr int NK = Cic5Cfg<HALO>::NK, CAP = Cic5Cfg<HALO>::CAP;
+    if (!in_domain<3>(g, x, y, z)) return 1;
+    float fx_, fy_, fz_;
+    const int fx = first_node<1>(x, fx_);
+    const int fy = first_node<1>(y, fy_);
+    const int fz = first_node<1>(z, fz_);
+    const int lx = local_index<2, 8, HALO>(fx, ox, g.N[0]);
+    const int ly = local_index<2, 8, HALO>(fy, oy, g.N[1]);
+    const int lz = local_index<2, 8, HALO>(fz, oz, g.N[2]);
+    const bool home = (lx >= C::KLO) & (lx < C::KHI) & (ly >= C::KLO) & (ly < C::KHI) & (lz >= C::KLO) &
+                      (lz < C::KHI);
+    if (home) {
+        const int k = ((lz - C::KLO) * C::KR + (ly - C::KLO)) * C::KR + (lx - C::KLO);
+        const unsigned r = atomicAdd(&cnt[k], 1u);
+        if (r < (unsigned)CAP) {
+            float2 *dst = st + r * NK + k;
+            dst[0] = make_float2(fx_, fy_);
+            dst[CAP * NK] = make_float2(fz_, qvx);
+            dst[2 * CAP * NK] = make_float2(qvy, qvz);
+            return 0;
+        }
+        // more than CAP in this cell: straight to J like a halo particle
+    } else {
+        const bool fits = (lx >= -HALO) & (lx + 1 < 8 + HALO) & (ly >= -HALO) & (ly + 1 < 8 + HALO) &
+                          (lz >= -HALO) & (lz + 1 < 8 + HALO);
+        if (!fits) {
+            deposit_global<3, 1>(g, J, x, y, z, qvx, qvy, qvz);
+            return 2;
+        }
+    }
+    stencil_to_global<HALO>(g, J, ox, oy, oz, lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
+    return 0;
 }
 
 template <int HALO>
@@ -613,20 +650,19 @@ __global__ void __launch_bounds__(512, 1)
                             float *__restrict__ J, Counters ctr, bool vec) {
     using K = Cic5Cfg<HALO>;
     using C = typename K::C;
-    constexpr int NK = K::NK, CAP = K::CAP, HCAP = K::HCAP;
+    constexpr int NK = K::NK, CAP = K::CAP, QCAP = K::QCAP;
     extern __shared__ __align__(16) unsigned char dsm[];
-    float2 *st = reinterpret_cast<float2 *>(dsm);                             // [3][CAP][NK]
-    float *hbuf = reinterpret_cast<float *>(st + 3 * CAP * NK);               // [7][HCAP]
-    unsigned *cnt = reinterpret_cast<unsigned *>(hbuf + 7 * HCAP);            // [NK]
-    __shared__ unsigned hcount[2];
+    float2 *st = reinterpret_cast<float2 *>(dsm);                              // [3][CAP][NK]
+    int *qbuf = reinterpret_cast<int *>(st + 3 * CAP * NK);                    // [warps][QCAP]
+    unsigned *cnt = reinterpret_cast<unsigned *>(qbuf + (K::THREADS / 32) * QCAP);  // [NK]
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
+    int *wq = qbuf + (tid >> 5) * QCAP;  // this warp's queue: particle offsets in the round
     unsigned n_esc = 0, n_inv = 0;
     const int kx0 = tid % C::KR + C::KLO, ky0 = (tid / C::KR) % C::KR + C::KLO,
               kz0 = tid / (C::KR * C::KR) + C::KLO;
 
     if (tid < NK) cnt[tid] = 0;
-    if (tid < 2) hcount[tid] = 0;
     float acc[8][3];
 #pragma unroll
     for (int a = 0; a < 8; ++a) acc[a][0] = acc[a][1] = acc[a][2] = 0.f;
@@ -688,24 +724,17 @@ __global__ void __launch_bounds__(512, 1)
     }
     load_round(cur);
     __syncthreads();  // counters zeroed
-    int parity = 0;
     int ox = 0, oy = 0, oz = 0;  // origin of the current tile
-    // a halo particle, or a grouped one beyond CAP: into this round's short list
-    auto to_list = [&](int lx, int ly, int lz, float fx, float fy, float fz, float qvx, float qvy, float qvz) {
-        const unsigned hs = atomicAdd(&hcount[parity], 1u);
-        if (hs < (unsigned)HCAP) {
-            hbuf[0 * HCAP + hs] = fx;
-            hbuf[1 * HCAP + hs] = fy;
-            hbuf[2 * HCAP + hs] = fz;
-            hbuf[3 * HCAP + hs] = qvx;
-            hbuf[4 * HCAP + hs] = qvy;
-            hbuf[5 * HCAP + hs] = qvz;
-            hbuf[6 * HCAP + hs] = __int_as_float(((lx + HALO) & 255) | (((ly + HALO) & 255) << 8) |
-                                                 (((lz + HALO) & 255) << 16));
-        } else {
-            list_full_to_global<HALO>(g, J, ox, oy, oz, lx, ly, lz, fx, fy, fz, qvx, qvy, qvz);
-        }
+    // A particle the fast path does not take (outside the tile's own cells, or
+    // beyond CAP in its cell, or invalid) is queued by its warp; the warp then
+    // takes its queue with one particle per lane: the general path runs once per
+    // warp instead of inside the unrolled loop whenever any lane needs it, and
+    // the global reductions of halo and overflow particles are issued there.
+    auto slow_count = [&](int rc) {
+        n_inv += rc == 1;
+        n_esc += rc == 2;
     };
+    const unsigned lanes_below = (1u << lane) - 1u;
     while (true) {
         // ---- place the round held in registers (tile cur.t, origin o*) ----
         const int tx = (int)(cur.t % (unsigned)g.nt[0]);
@@ -717,10 +746,11 @@ __global__ void __launch_bounds__(512, 1)
         // the tile's own cells that exist (a last tile may stick out of the grid)
         const unsigned limx = (unsigned)min(C::KHI, g.N[0] - ox), limy = (unsigned)min(C::KHI, g.N[1] - oy),
                        limz = (unsigned)min(C::KHI, g.N[2] - oz);
+        int qn = 0;  // particles this warp has queued this round (warp-uniform)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const long long p = cur.rb + (j >> 2) * (K::R / 2) + 4 * tid + (j & 3);
-            if (p < cur.lo || p >= cur.hi) continue;
+            const bool live = p >= cur.lo && p < cur.hi;
             const float x = X[j], y = Y[j], z = Z[j];
             const float qq = Q[j];
             const float qvx = qq * VX[j], qvy = qq * VY[j], qvz = qq * VZ[j];
@@ -728,57 +758,39 @@ __global__ void __launch_bounds__(512, 1)
             const int fx = first_node<1>(x, fx_);
             const int fy = first_node<1>(y, fy_);
             const int fz = first_node<1>(z, fz_);
-            {
-                // fast path: the cell is one of the tile's own cells inside the grid
-                // and the coordinates are not negative (the conversion truncates
-                // towards zero); then x, y, z are in the domain (a NaN fails too)
-                const unsigned dx = (unsigned)(fx - ox), dy = (unsigned)(fy - oy), dz = (unsigned)(fz - oz);
-                if ((C::KLO == 0) & (x >= 0.f) & (y >= 0.f) & (z >= 0.f) & (dx < limx) & (dy < limy) &
-                    (dz < limz)) {
-                    const int k = ((int)dz * C::KR + (int)dy) * C::KR + (int)dx;
-                    const unsigned r = atomicAdd(&cnt[k], 1u);
-                    if (r < (unsigned)CAP) {
-                        float2 *dst = st + r * NK + k;
-                        dst[0] = make_float2(fx_, fy_);
-                        dst[CAP * NK] = make_float2(fz_, qvx);
-                        dst[2 * CAP * NK] = make_float2(qvy, qvz);
-                    } else {
-                        to_list((int)dx, (int)dy, (int)dz, fx_, fy_, fz_, qvx, qvy, qvz);
-                    }
-                    continue;
-                }
-            }
-            if (!in_domain<3>(g, x, y, z)) {
-                ++n_inv;
-                continue;
-            }
-            const int lx = local_index<2, 8, HALO>(fx, ox, g.N[0]);
-            const int ly = local_index<2, 8, HALO>(fy, oy, g.N[1]);
-            const int lz = local_index<2, 8, HALO>(fz, oz, g.N[2]);
-            const bool home = (lx >= C::KLO) & (lx < C::KHI) & (ly >= C::KLO) & (ly < C::KHI) &
-                              (lz >= C::KLO) & (lz < C::KHI);
-            if (home) {
-                const int k = ((lz - C::KLO) * C::KR + (ly - C::KLO)) * C::KR + (lx - C::KLO);
+            // fast path: the cell is one of the tile's own cells inside the grid
+            // and the coordinates are not negative (the conversion truncates
+            // towards zero); then x, y, z are in the domain (a NaN fails too)
+            const unsigned dx = (unsigned)(fx - ox), dy = (unsigned)(fy - oy), dz = (unsigned)(fz - oz);
+            bool slow = live;
+            if (live & (C::KLO == 0) & (x >= 0.f) & (y >= 0.f) & (z >= 0.f) & (dx < limx) & (dy < limy) &
+                (dz < limz)) {
+                const int k = ((int)dz * C::KR + (int)dy) * C::KR + (int)dx;
                 const unsigned r = atomicAdd(&cnt[k], 1u);
                 if (r < (unsigned)CAP) {
                     float2 *dst = st + r * NK + k;
                     dst[0] = make_float2(fx_, fy_);
                     dst[CAP * NK] = make_float2(fz_, qvx);
                     dst[2 * CAP * NK] = make_float2(qvy, qvz);
-                    continue;
-                }
-                // more than CAP in this cell: listed below like a halo particle
-            } else {
-                const bool fits = (lx >= -HALO) & (lx + 1 < 8 + HALO) & (ly >= -HALO) & (ly + 1 < 8 + HALO) &
-                                  (lz >= -HALO) & (lz + 1 < 8 + HALO);
-                if (!fits) {
-                    ++n_esc;
-                    escape_to_global(g, J, x, y, z, qvx, qvy, qvz);
-                    continue;
+                    slow = false;
                 }
             }
-            to_list(lx, ly, lz, fx_, fy_, fz_, qvx, qvy, qvz);
+            const unsigned m = __ballot_sync(0xffffffffu, slow);
+            if (m) {  // warp-uniform
+                if (slow) wq[qn + __popc(m & lanes_below)] = (int)(p - cur.rb);
+                qn += __popc(m);
+            }
         }
+        // the warp's queue, one particle per lane: re-read from memory (it was
+        // loaded one round ago and sits in L2), then the general path
+        __syncwarp();
+        for (int e = lane; e < qn; e += 32) {
+            const long long pp = cur.rb + wq[e];
+            const float q = P.q[pp];
+            slow_count(slow_particle<HALO>(g, J, st, cnt, ox, oy, oz, P.x[pp], P.y[pp], P.z[pp], q * P.vx[pp],
+                                           q * P.vy[pp], q * P.vz[pp]));
+        }
+        __syncwarp();
         // ---- the next round: position, and its particles into registers ----
         RoundPos nxt = cur;
         nxt.rb = cur.rb + K::R;
@@ -789,7 +801,6 @@ __global__ void __launch_bounds__(512, 1)
         if (more) load_round(nxt);
 
         // ---- every cell's thread adds its staged particles in registers ----
-        if (tid == 0) hcount[parity ^ 1] = 0;  // the list the next round fills
         if (tid < NK) {
             const unsigned m0 = cnt[tid];
             const unsigned m = m0 < (unsigned)CAP ? m0 : (unsigned)CAP;
@@ -812,16 +823,6 @@ __global__ void __launch_bounds__(512, 1)
                 }
             }
         }
-        {
-            const unsigned nh = min(hcount[parity], (unsigned)HCAP);
-            for (unsigned h = tid; h < nh; h += K::THREADS) {
-                const int pk = __float_as_int(hbuf[6 * HCAP + h]);
-                stencil_to_global<HALO>(g, J, ox, oy, oz, (pk & 255) - HALO, ((pk >> 8) & 255) - HALO,
-                                        ((pk >> 16) & 255) - HALO, hbuf[h], hbuf[HCAP + h], hbuf[2 * HCAP + h],
-                                        hbuf[3 * HCAP + h], hbuf[4 * HCAP + h], hbuf[5 * HCAP + h]);
-            }
-        }
-        parity ^= 1;
         if (tile_ends) {
             // The tile's flush without shared-memory float atomics: every cell's 8
             // corners x 3 components go to the (now free) staging area with plain
