@@ -797,8 +797,10 @@ __global__ void __launch_bounds__(512, 1)
         if (nxt.rb >= cur.hi) seek(g, offs, chunk_tile, n, chunk, nchunks, cur.c, cur.t + 1, nxt);
         const bool tile_ends = nxt.t != cur.t || nxt.c != cur.c;
         const bool more = nxt.t < g.n_tiles;
-        __syncthreads();  // the round is staged
+        // the next round's loads go out before the barrier, so that the warps
+        // issue them as they finish placing instead of all at once after it
         if (more) load_round(nxt);
+        __syncthreads();  // the round is staged
 
         // ---- every cell's thread adds its staged particles in registers ----
         if (tid < NK) {
