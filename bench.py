@@ -761,7 +761,11 @@ def run_only(args):
         out = zigzag_workload(pcg, synth.zigzag3d(grid=(args.zz_grid,) * 3), args.steps, args.warmup, dist, peaks,
                               traffic)
     else:
-        d = synth.quad3d_bump() if args.only == "quad" else synth.cic2d()
+        if args.only == "quad":
+            qg = args.quad_grid
+            d = synth.quad3d_bump(grid=(qg, qg, qg), sigma_bump=16.0 * qg / 192)
+        else:
+            d = synth.cic2d()
         out = current_workload(pcg, d, args.steps, args.warmup, dist, peaks, traffic)
         out.pop("profile", None)
     print(json.dumps({"only": args.only, **out}), flush=True)
@@ -831,6 +835,8 @@ def main():
                     help="time one secondary workload alone and print its figures (for profiling)")
     ap.add_argument("--mass-grid", type=int, default=64, help="edge of the mass-matrix grid")
     ap.add_argument("--zz-grid", type=int, default=256, help="edge of the zigzag grid (--only zigzag)")
+    ap.add_argument("--quad-grid", type=int, default=192,
+                    help="edge of the quadratic bump grid (--only quad; the bump's width scales with it)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
