@@ -64,6 +64,16 @@ typedef struct pcg_stats {
 #define PCG_FLAG_TIMEOUT 4u       /* a bounded wait for an asynchronous copy or a tensor-core result
                                      gave up; the call's output is invalid */
 
+/* Index checks.  The library built with -DPCG_CHECKED (the checked build)
+ * tests the data-dependent indices of its kernels (from positions, offsets,
+ * counts and ranks) before each access they guard; a failed test skips the
+ * access and adds one to a device counter (no trap, no assert).  This call
+ * synchronises the device, stores the failures counted since the previous call
+ * in *failures (HOST) and resets the count; *checked_build (HOST, may be NULL)
+ * is set to 1 in the checked build, else 0 (and *failures to 0).
+ * PCG_ERR_INVALID_ARG for a NULL failures pointer. */
+PCG_API pcg_status pcg_bounds_check_failures(uint64_t *failures, int32_t *checked_build);
+
 /* Library version (major * 10000 + minor * 100 + patch). */
 PCG_API int pcg_version(void);
 

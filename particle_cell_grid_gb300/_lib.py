@@ -27,6 +27,7 @@ SIGNATURES = {
     "pcg_version": (ctypes.c_int, []),
     "pcg_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "pcg_stats_check": (ctypes.c_int, [_vp]),
+    "pcg_bounds_check_failures": (ctypes.c_int, [_P(ctypes.c_uint64), _P(_i32)]),
     "pcg_deposit_cic1d": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i32, _i32, _dbl, _dbl, _vp, _vp, _vp]),
     "pcg_deposit_cic1d_grad": (ctypes.c_int, [_vp, _vp, _i64, _vp, _i32, _i32, _dbl, _dbl, _vp, _vp, _vp, _vp]),
     "pcg_tile_sort_workspace_size": (ctypes.c_int, [_i32, _vp, _i32, _i64, _i32, _P(_sz)]),
@@ -53,7 +54,9 @@ class PcgError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB
+    """libpcg.so of this package; PCG_LIBRARY selects another build of the same
+    library (e.g. the checked build, particle_cell_grid_gb300/_build_checked)."""
+    return os.environ.get("PCG_LIBRARY") or _build.LIB
 
 
 def load() -> ctypes.CDLL:

@@ -1,7 +1,22 @@
-// api.cu -- version, status strings, stats check and the fill kernel.
+// api.cu -- version, status strings, stats check, the index-check counters
+// and the fill kernel.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace pcg {
+
+namespace {
+std::mutex g_check_mu;
+CheckReader g_check_readers[64];
+int g_check_n = 0;
+}  // namespace
+
+int check_register(CheckReader reader) {
+    std::lock_guard<std::mutex> lock(g_check_mu);
+    if (g_check_n < 64) g_check_readers[g_check_n++] = reader;
+    return g_check_n;
+}
 
 // Grid-stride zero fill; 16-byte stores on the aligned body.
 __global__ void __launch_bounds__(256) zero_f32_kernel(float *__restrict__ p, size_t count) {
@@ -49,5 +64,26 @@ extern "C" const char *pcg_status_string(int status) {
 extern "C" pcg_status pcg_stats_check(const pcg_stats *s) {
     if (s == nullptr) return PCG_ERR_INVALID_ARG;
     if (s->n_invalid != 0 || s->error_flags != 0) return PCG_ERR_DOMAIN;
+    return PCG_OK;
+}
+
+extern "C" pcg_status pcg_bounds_check_failures(uint64_t *failures, int32_t *checked_build) {
+    if (failures == nullptr) return PCG_ERR_INVALID_ARG;
+#ifdef PCG_CHECKED
+    const int32_t checked = 1;
+#else
+    const int32_t checked = 0;
+#endif
+    if (checked_build) *checked_build = checked;
+    uint64_t total = 0;
+    if (checked) {
+        if (cudaDeviceSynchronize() != cudaSuccess) {
+            (void)cudaGetLastError();
+            return PCG_ERR_CUDA;
+        }
+        std::lock_guard<std::mutex> lock(pcg::g_check_mu);
+        for (int i = 0; i < pcg::g_check_n; ++i) total += pcg::g_check_readers[i]();
+    }
+    *failures = total;
     return PCG_OK;
 }

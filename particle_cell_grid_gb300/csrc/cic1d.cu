@@ -250,6 +250,7 @@ __device__ __forceinline__ void cic1d_deposit_pair(const Cic1dArgs &a, const dou
                                                    float vf, int t) {
     Pair pr;
     if (!cic1d_select(a, ctab, xf, vf, t, pr)) return;
+    if (!PCG_IN(pr.b0, a.nbins) || !PCG_IN(pr.b1, a.nbins)) return;
     red_shared_add_f32(&hist[pr.b0], pr.w * (1.f - pr.f));
     red_shared_add_f32(&hist[pr.b1], pr.w * pr.f);
 }
@@ -366,6 +367,7 @@ __global__ void __launch_bounds__(kThreads)
         [&](float xf, float vf, int t, long long p) {
             Pair pr;
             if (!cic1d_select(a, ctab, xf, vf, t, pr)) return;
+            if (!PCG_IN(pr.b0, a.nbins) || !PCG_IN(pr.b1, a.nbins) || !PCG_IN(p, a.n)) return;
             const float dw = -2.f * pr.u * pr.sgn * a.inv_hw32;
             const float G0 = 2.f * (H[pr.b0] - a.target[pr.b0]);
             const float G1 = 2.f * (H[pr.b1] - a.target[pr.b1]);

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include "../../include/pcg.h"
+#include "checked.cuh"
 #include "profile.cuh"
 
 #define PCG_VERSION_NUMBER 100  // 0.1.0

@@ -94,6 +94,7 @@ __device__ __forceinline__ void deposit_global(const Geom &g, float *__restrict_
 #pragma unroll
             for (int kx = 0; kx < S; ++kx) {
                 const long long node = row + wrap_index(fx + kx, g.N[0]);
+                if (!PCG_IN(node, g.ncells)) continue;
                 const float W = wyz * wx[kx];
                 red_add_f32(J + node, qvx * W);
                 red_add_f32(J + g.ncells + node, qvy * W);

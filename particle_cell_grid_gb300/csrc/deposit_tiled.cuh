@@ -140,6 +140,7 @@ __device__ __forceinline__ void scratch_particle(float *scratch, int lx, int ly,
     if (DIM == 3) weights_from<ORDER>(tz, wz);
     else wz[0] = 1.f;
     const int base = ((DIM == 3 ? (lz + HALO) * C::TE : 0) + (ly + HALO)) * C::TE + (lx + HALO);
+    if (!PCG_IN(base, C::CELLS) || !PCG_IN(base + ((C::SZ - 1) * C::TE + S - 1) * C::TE + S - 1, C::CELLS)) return;
 #pragma unroll
     for (int kz = 0; kz < C::SZ; ++kz)
 #pragma unroll
@@ -179,12 +180,10 @@ __device__ __forceinline__ void flush_scratch(const Geom &g, const float *scratc
             // a grid shorter than the window: wrap each cell on its own
             for (int sx = 0; sx < C::TE; ++sx) {
                 const float v = scratch[row * C::TE + sx];
-                if (v != 0.f)
-                    red_add_f32(J + c * g.ncells +
-                                    ((long long)wrap_index(oz - HALO + sz, g.N[2]) * g.N[1] +
-                                     wrap_index(oy - HALO + sy, g.N[1])) * g.N[0] +
-                                    wrap_index(ox - HALO + sx, g.N[0]),
-                                v);
+                const long long node = ((long long)wrap_index(oz - HALO + sz, g.N[2]) * g.N[1] +
+                                        wrap_index(oy - HALO + sy, g.N[1])) * g.N[0] +
+                                       wrap_index(ox - HALO + sx, g.N[0]);
+                if (v != 0.f && PCG_IN(node, g.ncells)) red_add_f32(J + c * g.ncells + node, v);
             }
             continue;
         }
@@ -202,6 +201,7 @@ __device__ __forceinline__ void flush_scratch(const Geom &g, const float *scratc
             }
             int run = g.N[0] - gx;            // contiguous in J up to the wrap
             if (run > C::TE - sx) run = C::TE - sx;
+            if (!PCG_IN(((long long)gz * g.N[1] + gy) * g.N[0] + gx + run - 1, g.ncells)) break;
             float *dst = jrow + gx;
             const float *sv = src + sx;
             int k = 0;
@@ -346,7 +346,8 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
                         qv[slot][0] = qvx;
                         qv[slot][1] = qvy;
                         qv[slot][2] = qvz;
-                        atomicAdd(&cnt[k], 1u);
+                        if (PCG_IN(k, NK)) atomicAdd(&cnt[k], 1u);
+                        else key[slot] = 0xffffffffu;
                         continue;
                     }
                     bool fits = (lx >= -HALO) & (lx + S - 1 < TILE + HALO) & (ly >= -HALO) &
@@ -360,6 +361,7 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
                     // drifted into the halo: listed at the top of the staging
                     // buffer and deposited after the groups by densely packed threads
                     const unsigned hs = BC::SB - 1 - atomicAdd(&n_halo, 1u);
+                    if (!PCG_IN(hs, BC::SB)) continue;
                     stage[0 * BC::SB + hs] = tx_;
                     stage[1 * BC::SB + hs] = ty_;
                     stage[2 * BC::SB + hs] = tz_;
@@ -385,6 +387,7 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
             for (int i = 0; i < BC::PPT; ++i) {
                 if (key[i] == 0xffffffffu) continue;
                 const unsigned slot = atomicAdd(&cur[key[i]], 1u);
+                if (!PCG_IN(slot, BC::SB)) continue;
                 stage[0 * BC::SB + slot] = off[i][0];
                 stage[1 * BC::SB + slot] = off[i][1];
                 stage[2 * BC::SB + slot] = off[i][2];
@@ -416,6 +419,7 @@ __global__ void __launch_bounds__(THREADS, 512 / THREADS)
                 const unsigned m = cnt[k];
                 if (m == 0) continue;
                 const unsigned b0 = start[k];
+                if (!PCG_IN(b0 + m - 1, BC::SB)) continue;
                 float acc[C::SZ][S][S][3];
 #pragma unroll
                 for (int kz = 0; kz < C::SZ; ++kz)
@@ -588,6 +592,7 @@ __device__ __forceinline__ void stencil_to_global(const Geom &g, float *__restri
 #pragma unroll
             for (int kx = 0; kx < 2; ++kx) {
                 const float W = wyz * wx[kx];
+                if (!PCG_IN(row + gx[kx], g.ncells)) continue;
                 float *j = J + row + gx[kx];
                 red_add_f32(j, qvx * W);
                 red_add_f32(j + g.ncells, qvy * W);
@@ -622,6 +627,7 @@ __device__ __forceinline__ int slow_particle(const Geom &g, float *J, float2 *st
                       (lz < C::KHI);
     if (home) {
         const int k = ((lz - C::KLO) * C::KR + (ly - C::KLO)) * C::KR + (lx - C::KLO);
+        if (!PCG_IN(k, NK)) return 0;
         const unsigned r = atomicAdd(&cnt[k], 1u);
         if (r < (unsigned)CAP) {
             float2 *dst = st + r * NK + k;
@@ -766,7 +772,7 @@ __global__ void __launch_bounds__(512, 1)
             if (live & (C::KLO == 0) & (x >= 0.f) & (y >= 0.f) & (z >= 0.f) & (dx < limx) & (dy < limy) &
                 (dz < limz)) {
                 const int k = ((int)dz * C::KR + (int)dy) * C::KR + (int)dx;
-                const unsigned r = atomicAdd(&cnt[k], 1u);
+                const unsigned r = PCG_IN(k, NK) ? atomicAdd(&cnt[k], 1u) : (unsigned)CAP;
                 if (r < (unsigned)CAP) {
                     float2 *dst = st + r * NK + k;
                     dst[0] = make_float2(fx_, fy_);
@@ -777,7 +783,7 @@ __global__ void __launch_bounds__(512, 1)
             }
             const unsigned m = __ballot_sync(0xffffffffu, slow);
             if (m) {  // warp-uniform
-                if (slow) wq[qn + __popc(m & lanes_below)] = (int)(p - cur.rb);
+                if (slow && PCG_IN(qn + __popc(m & lanes_below), QCAP)) wq[qn + __popc(m & lanes_below)] = (int)(p - cur.rb);
                 qn += __popc(m);
             }
         }
@@ -786,6 +792,7 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
         for (int e = lane; e < qn; e += 32) {
             const long long pp = cur.rb + wq[e];
+            if (!PCG_IN(pp, n)) continue;
             const float q = P.q[pp];
             slow_count(slow_particle<HALO>(g, J, st, cnt, ox, oy, oz, P.x[pp], P.y[pp], P.z[pp], q * P.vx[pp],
                                            q * P.vy[pp], q * P.vz[pp]));
@@ -868,6 +875,7 @@ __global__ void __launch_bounds__(512, 1)
                 while (gy >= g.N[1]) gy -= g.N[1];
                 while (gz >= g.N[2]) gz -= g.N[2];
                 const long long node = ((long long)gz * g.N[1] + gy) * g.N[0] + gx;
+                if (!PCG_IN(node, g.ncells)) continue;
 #pragma unroll
                 for (int comp = 0; comp < 3; ++comp)
                     if (sum[comp] != 0.f) red_add_f32(J + comp * g.ncells + node, sum[comp]);

@@ -156,7 +156,8 @@ __device__ __forceinline__ void zigzag_global(const Geom &g, float *__restrict__
         const int gx = wrap_once(z.base[0] + dx, g.N[0]);
         const int gy = wrap_once(z.base[1] + dy, g.N[1]);
         const int gz = wrap_once(z.base[2] + dz, g.N[2]);
-        red_add_f32(J + c * g.ncells + ((long long)gz * g.N[1] + gy) * g.N[0] + gx, v);
+        const long long node = ((long long)gz * g.N[1] + gy) * g.N[0] + gx;
+        if (PCG_IN(node, g.ncells)) red_add_f32(J + c * g.ncells + node, v);
     });
 }
 
@@ -210,7 +211,9 @@ __device__ __noinline__ void zigzag_general(const Geom g, const ZParticles P, lo
         zigzag_global(g, J, z);
         return;
     }
-    float *w0 = scratch + ((lz + HALO) * TE + (ly + HALO)) * TE + (lx + HALO);
+    const int b0 = ((lz + HALO) * TE + (ly + HALO)) * TE + (lx + HALO);
+    if (!PCG_IN(b0, C::CELLS) || !PCG_IN(b0 + (2 * TE + 2) * TE + 2, C::CELLS)) return;
+    float *w0 = scratch + b0;
     zigzag_edges(z, [&](int c, int dx, int dy, int dz, float v) {
         red_shared_add_f32(w0 + c * C::CELLS + (dz * TE + dy) * TE + dx, v);
     });
@@ -326,7 +329,9 @@ __global__ void __launch_bounds__(256, 3)
                 mid[mu] = 0.5f * (f1[mu] + f2[mu]);
                 F[mu] = q * D[mu] * inv_dt;
             }
-            float *w0 = scratch + ((lz + HALO) * TE + (ly + HALO)) * TE + (lx + HALO);
+            const int b0 = ((lz + HALO) * TE + (ly + HALO)) * TE + (lx + HALO);
+            if (!PCG_IN(b0, C::CELLS) || !PCG_IN(b0 + (TE + 1) * TE + 1, C::CELLS)) continue;
+            float *w0 = scratch + b0;
 #pragma unroll
             for (int c = 0; c < 3; ++c) {
                 const int u = (c + 1) % 3, v = (c + 2) % 3;

@@ -119,6 +119,7 @@ __device__ void particle_global(const Args &A, float x, float y, float z, float 
             const int o = (((b >> 2) - (a >> 2)) + 1) * 9 + ((((b >> 1) & 1) - ((a >> 1) & 1)) + 1) * 3 +
                           ((b & 1) - (a & 1)) + 1;
             const float WW = Wa * corner_w(b, fx, fy, fz);
+            if (!PCG_IN(g, A.ncells)) continue;
             for (int c = 0; c < NC; ++c) red_add_f32(A.M + (g * 27 + o) * NC + c, s[c] * WW);
         }
     }
@@ -278,6 +279,7 @@ __device__ __forceinline__ void flush_window(const Args &A, const float *acc, co
             if (gx0 >= A.N[0]) gx0 -= A.N[0];
             int len = WNX - nx0;
             if (gx0 + len > A.N[0]) len = A.N[0] - gx0;  // the row wraps at the x boundary
+            if (!PCG_IN(((long long)gz * A.N[1] + gy) * A.N[0] + gx0 + len - 1, A.ncells)) break;
             float *dst = A.M + (((long long)gz * A.N[1] + gy) * A.N[0] + gx0) * NB;
             const float *sp = src + nx0 * NB;
             const int L = len * NB;

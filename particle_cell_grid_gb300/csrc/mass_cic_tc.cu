@@ -409,7 +409,10 @@ __global__ void __launch_bounds__(kPThreads, 1) mass_tc_kernel(Args A) {
                         const int nx = ci % BCX + (a & 1), ny = (ci / BCX) % BCY + ((a >> 1) & 1),
                                   nz = ci / (BCX * BCY) + (a >> 2);
                         const int wr = nz * WNY + ny;
-                        float *base = acc + wr * ACC_ROW + rsh[wr] + nx * NB + c - (pa - 13) * NC;
+                        const int bi = wr * ACC_ROW + rsh[wr] + nx * NB + c - (pa - 13) * NC;
+                        // partners at base + P(nn) NC, P(nn) in [0, 13]
+                        if (!PCG_IN(bi, ACC_FLOATS) || !PCG_IN(bi + 13 * NC, ACC_FLOATS)) continue;
+                        float *base = acc + bi;
                         float old[8];
 #pragma unroll
                         for (int nn = 0; nn < 8; ++nn)

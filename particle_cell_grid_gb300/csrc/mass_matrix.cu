@@ -113,12 +113,16 @@ __global__ void __launch_bounds__(kThreads, 2) mass_simt_kernel(Args A) {
                 const int ci = bt[jj].ci;
                 const int nx = ci % BCX + (a & 1), ny = (ci / BCX) % BCY + ((a >> 1) & 1), nz = ci / (BCX * BCY) + (a >> 2);
                 const int wr = nz * WNY + ny;
-                float *row = acc + wr * ACC_ROW + rsh[wr] + nx * NB + c;
+                const int ri = wr * ACC_ROW + rsh[wr] + nx * NB + c;
+                float *row = acc + ri;
+                // (no early exit here: the barrier below is reached by every thread)
+                if (PCG_IN(ri, ACC_FLOATS) && PCG_IN(ri + 26 * NC, ACC_FLOATS)) {
 #pragma unroll
-                for (int nn = 0; nn < 8; ++nn) {
-                    const int o = ((nn >> 2) - (a >> 2) + 1) * 9 + (((nn >> 1) & 1) - ((a >> 1) & 1) + 1) * 3 +
-                                  ((nn & 1) - (a & 1) + 1);
-                    red_shared_add_f32(row + o * NC, d[nn]);
+                    for (int nn = 0; nn < 8; ++nn) {
+                        const int o = ((nn >> 2) - (a >> 2) + 1) * 9 + (((nn >> 1) & 1) - ((a >> 1) & 1) + 1) * 3 +
+                                      ((nn & 1) - (a & 1) + 1);
+                        red_shared_add_f32(row + o * NC, d[nn]);
+                    }
                 }
             }
             __syncthreads();  // staging and the batch list are reused

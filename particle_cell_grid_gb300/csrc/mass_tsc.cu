@@ -62,7 +62,7 @@ __global__ void mirror_kernel(float *__restrict__ M, int Nx, int Ny, int Nz, lon
         const int dx = o % 5 - 2, dy = (o / 5) % 5 - 2, dz = o / 25 - 2;
         const int gx = (int)(g % Nx), gy = (int)((g / Nx) % Ny), gz = (int)(g / ((long long)Nx * Ny));
         const long long gp = ((long long)wrapi(gz + dz, Nz) * Ny + wrapi(gy + dy, Ny)) * Nx + wrapi(gx + dx, Nx);
-        M[(g * 125 + o) * 9 + c] = M[(gp * 125 + (124 - o)) * 9 + c];
+        if (PCG_IN(gp, ncells)) M[(g * 125 + o) * 9 + c] = M[(gp * 125 + (124 - o)) * 9 + c];
     }
 }
 

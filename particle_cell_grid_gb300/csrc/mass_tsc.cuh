@@ -58,6 +58,7 @@ static __device__ __noinline__ void particle_global(const Args A, float x, float
         const long long g = ((long long)wrapi(fz + az, A.N[2]) * A.N[1] + wrapi(fy + ay, A.N[1])) * A.N[0] +
                             wrapi(fx + ax, A.N[0]);
         const float Wa = wx[ax] * wy[ay] * wz[az];
+        if (!PCG_IN(g, A.ncells)) continue;
         for (int b = 0; b < 27; ++b) {
             const int bx = b % 3, by = (b / 3) % 3, bz = b / 9;
             const int o = (bz - az + 2) * 25 + (by - ay + 2) * 5 + (bx - ax + 2);
@@ -120,6 +121,7 @@ __device__ __forceinline__ void flush_slot(float *M, long long total, float *slo
     float4 *q = reinterpret_cast<float4 *>(slot);
 #pragma unroll
     for (int i = 0; i < kSlot / 4; ++i) q[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    active = active && PCG_IN(start, total) && PCG_IN(start + L - 1, total);
     const int mis = (int)(start & 3);
 #pragma unroll
     for (int k = 0; k < 36; ++k)

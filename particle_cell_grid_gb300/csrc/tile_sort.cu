@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kSortThreads)
         for (int u = 0; u < U; ++u) {
             if (q + (long long)u * blockDim.x >= p1) break;
             const unsigned k = tile_key<DIM, TILE>(g, x[u], y[u], z[u]);
-            atomicAdd(&hist[k], 1u);
+            if (PCG_IN(k, B)) atomicAdd(&hist[k], 1u);
             inval += (k == g.n_tiles);
         }
     }
@@ -181,7 +181,9 @@ __global__ void __launch_bounds__(kSortThreads)
     const long long p1 = min(n, p0 + chunk);
     for (long long p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
         const unsigned k = tile_key<DIM, TILE>(g, kx[p], ky[p], DIM == 3 ? kz[p] : 0.f);
+        if (!PCG_IN(k, B)) continue;
         const unsigned slot = atomicAdd(&cursor[k], 1u);
+        if (!PCG_IN(slot, n)) continue;
         for (int f = 0; f < np; ++f) pl.out[f][slot] = pl.in[f][p];
     }
 }
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(256)
     for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n;
          p += (long long)gridDim.x * blockDim.x) {
         const unsigned k = tile_key<DIM, TILE>(g, kx[p], ky[p], DIM == 3 ? kz[p] : 0.f);
-        atomicAdd(&totals[k], 1u);
+        if (PCG_IN(k, g.n_tiles + 1u)) atomicAdd(&totals[k], 1u);
         inval += (k == g.n_tiles);
     }
     warp_add_u64(n_invalid, inval);
@@ -209,7 +211,9 @@ __global__ void __launch_bounds__(256)
     for (long long p = blockIdx.x * (long long)blockDim.x + threadIdx.x; p < n;
          p += (long long)gridDim.x * blockDim.x) {
         const unsigned k = tile_key<DIM, TILE>(g, kx[p], ky[p], DIM == 3 ? kz[p] : 0.f);
+        if (!PCG_IN(k, g.n_tiles + 1u)) continue;
         const unsigned slot = atomicAdd(&cursor[k], 1u);
+        if (!PCG_IN(slot, n)) continue;
         for (int f = 0; f < np; ++f) pl.out[f][slot] = pl.in[f][p];
     }
 }
@@ -471,6 +475,7 @@ __global__ void __launch_bounds__(kPartThreads, 1)
         for (unsigned slot = tid; slot < cur.len; slot += kPartThreads) {
             const unsigned i = perm[slot], d = sdig[slot];
             const unsigned gpos = gbase[d] + (slot - lstart[d]);
+            if (!PCG_IN(gpos, n) || !PCG_IN(i, cur.len)) continue;
             const unsigned *src = st + sh + i;
             if (PASS == 2) {
                 // measured faster for pass 2: one load-store pair per field

@@ -178,3 +178,11 @@ def test_tsc_mass_rejects_small_grids_and_bad_precisions(lib):
     assert f(_grid(8, 8, 8), 3, 2, 10, arr, vp, arr, vp, vp, None, None, 0, None) == 1  # order 3
     assert f(_grid(8, 8, 8), 2, -1, 10, arr, vp, arr, vp, vp, None, None, 0, None) == 1  # precision
     assert f(_grid(8, 8, 8), 2, 0, 10, arr, vp, arr, vp, ctypes.c_void_p(4100), None, None, 0, None) == 1  # M align
+
+
+def test_bounds_check_query_of_the_unchecked_build(lib):
+    failures = ctypes.c_uint64(7)
+    checked = ctypes.c_int32(-1)
+    assert lib.pcg_bounds_check_failures(ctypes.byref(failures), ctypes.byref(checked)) == 0
+    assert checked.value == 0 and failures.value == 0
+    assert lib.pcg_bounds_check_failures(None, None) == 1
