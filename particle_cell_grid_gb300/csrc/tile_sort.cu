@@ -19,7 +19,10 @@
 //  * B > kSmemBins (for example one bin per cell of a 64^3 grid): counts and
 //    cursors live in global memory and are bumped with global atomics.
 // No step waits on another CTA; kernel boundaries order the phases.
+#include <cmath>
+
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace pcg {
 namespace {
@@ -222,53 +225,82 @@ __global__ void __launch_bounds__(256)
 // Two-pass partition for outputs larger than L2 (MSD order).
 // Pass 1 moves every particle into one of <= 256 coarse buckets of `tpb`
 // consecutive tiles, pass 2 into its tile inside the bucket.  One persistent
-// CTA per SM walks batches of `bs` consecutive particles (<= 2048), two at a
-// time in flight:
-//  * the next batch's payload and key inputs go global -> shared with
-//    asynchronous copies (16 bytes where the arrays are aligned), never through
-//    registers, while the current batch is ranked and written;
-//  * the digits are counted in shared memory; the counting atomic's return
-//    value is the particle's rank inside its digit;
-//  * one global atomic per non-empty digit reserves a contiguous output range;
-//  * a 16-bit permutation lists the batch in digit order, and consecutive
-//    threads write consecutive output slots, so every digit's run leaves the SM
-//    as contiguous stores and the open sectors are one per bucket or tile
-//    frontier.
-constexpr int kPartThreads = 512;
-constexpr int kMaxBatch = 2048;
-constexpr int kItems = kMaxBatch / kPartThreads;
+// CTA per SM walks batches of `bs` consecutive input rows (4096 where shared
+// memory allows), dealt round-robin:
+//  * a producer warp copies the batch's fields global -> shared, one bulk
+//    (TMA) copy per field, into a single staging buffer, and refills a field
+//    for the next batch as soon as every worker warp has finished reading it
+//    (an mbarrier per field each way: "full" when the copy has landed, "free"
+//    when the 16 worker warps are done with it).  The key inputs come first,
+//    so the next batch can be ranked while this one is still being written;
+//  * 16 worker warps count the digits in shared memory (the counting atomic's
+//    return value is the particle's rank inside its digit), scan them, reserve
+//    one contiguous output run per non-empty digit with one global atomic, and
+//    list the batch in digit order in a 16-bit permutation;
+//  * consecutive threads then write consecutive output slots field by field,
+//    so every digit's run leaves the SM as contiguous stores, and the open
+//    sectors are one per bucket or tile frontier (the runs of successive
+//    batches, from any CTA, abut).
+// Measured on GB300: the store phase costs about the same per run of a digit
+// whatever its length, so the batch is as large as shared memory allows.
+// Every mbarrier wait is bounded; a timeout sets PCG_FLAG_TIMEOUT, and the
+// workers leave together at their next barrier (before any further global
+// write), the producer after its copies in flight have landed.
+constexpr int kPartWorkers = 512;
+constexpr int kPartThreads = kPartWorkers + 32;  // + the producer warp
+constexpr int kWorkerWarps = kPartWorkers / 32;
+constexpr int kMaxBatch = 4096;
+constexpr int kItems = kMaxBatch / kPartWorkers;
 constexpr unsigned kMaxPassBins = 2048;
 constexpr unsigned kMaxBuckets = 256;
+constexpr int kMaxRows = kMaxPayload + 3;
+constexpr uint32_t kPartPolls = 1u << 20;  // bounded waits: about 1 s with the 1 us suspend hint
+constexpr uint32_t kPartSleepNs = 1000;
+constexpr int kWorkBar = 1;  // named barrier of the worker warps
 
-__device__ __forceinline__ void cp_async4(unsigned *sdst, const unsigned *gsrc) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
-                     static_cast<unsigned>(__cvta_generic_to_shared(sdst))),
-                 "l"(gsrc)
+__device__ __forceinline__ void work_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kWorkBar), "n"(kPartWorkers) : "memory");
+}
+// OR over the worker threads, the same in all of them (and a worker barrier)
+__device__ __forceinline__ bool work_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kWorkBar), "n"(kPartWorkers)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_addr(mbar)), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async16(unsigned *sdst, const unsigned *gsrc) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                     static_cast<unsigned>(__cvta_generic_to_shared(sdst))),
-                 "l"(gsrc)
-                 : "memory");
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// global -> shared, completing on `mbar`'s transaction count.
+__device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            tc::smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(tc::smem_addr(mbar))
+        : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most one committed group of this thread is still in flight.
-__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
 
-// Exclusive scan of v[0..nb) in place (nb <= kMaxPassBins) by one CTA of
-// kPartThreads threads.
-__device__ void block_exclusive_scan(unsigned *v, unsigned nb, unsigned *warp_tot) {
-    constexpr int PER = kMaxPassBins / kPartThreads;
-    constexpr int NW = kPartThreads / 32;
+// out[0..nb) = exclusive scan of in[0..nb) (nb <= kMaxPassBins) by the worker
+// warps; in is read after the caller's barrier, out is ready after the last one.
+__device__ void work_exclusive_scan(const unsigned *in, unsigned *out, unsigned nb, unsigned *warp_tot) {
+    constexpr int PER = kMaxPassBins / kPartWorkers;
     const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned loc[PER];
     unsigned sum = 0;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const unsigned b = threadIdx.x * PER + i;
-        loc[i] = b < nb ? v[b] : 0u;
+        loc[i] = b < nb ? in[b] : 0u;
         sum += loc[i];
     }
     unsigned incl = sum;
@@ -278,56 +310,47 @@ __device__ void block_exclusive_scan(unsigned *v, unsigned nb, unsigned *warp_to
         if (lane >= (unsigned)o) incl += t;
     }
     if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
+    work_sync();
     if (warp == 0) {
-        const unsigned w = lane < NW ? warp_tot[lane] : 0u;
+        const unsigned w = lane < (unsigned)kWorkerWarps ? warp_tot[lane] : 0u;
         unsigned wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const unsigned t = __shfl_up_sync(0xffffffffu, wi, o);
             if (lane >= (unsigned)o) wi += t;
         }
-        if (lane < NW) warp_tot[lane] = wi - w;
+        if (lane < (unsigned)kWorkerWarps) warp_tot[lane] = wi - w;
     }
-    __syncthreads();
+    work_sync();
     unsigned run = warp_tot[warp] + incl - sum;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
         const unsigned b = threadIdx.x * PER + i;
-        if (b < nb) v[b] = run;
+        if (b < nb) out[b] = run;
         run += loc[i];
     }
-    __syncthreads();
+    work_sync();
 }
 
-// Copy elements [b0, b0 + len) of one 32-bit array (n_arr elements) into
-// stage[sh + i], sh = b0 % 4: 16-byte copies where the array is 16-byte aligned
-// and the whole vector lies inside the array, 4-byte copies otherwise.  The
-// stage row holds len + 4 elements.
-__device__ __forceinline__ void stage_field(unsigned *stage, const unsigned *__restrict__ src,
-                                            long long b0, unsigned len, long long n_arr) {
-    const int sh = (int)(b0 & 3);
-    const long long a0 = b0 - sh;
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-        const unsigned nv = (unsigned)(sh + len + 3) / 4;
-        for (unsigned v = threadIdx.x; v < nv; v += kPartThreads) {
-            const long long a = a0 + 4ll * v;
-            if (a + 4 <= n_arr) {
-                cp_async16(stage + 4 * v, src + a);
-            } else {
-                for (int e = 0; e < 4; ++e)
-                    if (a + e < n_arr) cp_async4(stage + 4 * v + e, src + a + e);
-            }
-        }
-    } else {
-        for (unsigned i = threadIdx.x; i < len; i += kPartThreads)
-            cp_async4(stage + sh + i, src + b0 + i);
-    }
-}
-
+// One batch: input rows [b0, b0 + len), digits [base, base + nb).
 struct BatchGeo {
     long long b0;
     unsigned len, base, nb;
+};
+
+struct PartArgs {
+    KeyGeom g;
+    const float *kx, *ky, *kz;
+    long long n;
+    Payload pl;
+    int np;
+    const unsigned *in_key;     // pass 2: tile keys written by pass 1
+    unsigned *out_key;          // pass 1 of two: tile keys for pass 2
+    const uint32_t *offs;       // tile offsets (bin starts)
+    unsigned *gcursor;          // next free output slot per bin (pass 1: per bucket)
+    const unsigned *batch_off;  // pass 2: first batch of each bucket
+    unsigned *flags;            // pcg_stats error flags (may be null)
+    unsigned tpb, B, nb1, nbcap, bs, nbatch;
 };
 
 // PASS 1: digit = bucket of the tile key computed from key positions; writes the
@@ -335,186 +358,261 @@ struct BatchGeo {
 //         payload straight to the output when one pass suffices).
 // PASS 2: digit = tile inside the batch's bucket; key read from the
 //         intermediate arrays; writes the final payload.
-// Shared memory: two buffers of nl = np + NK rows of (bs + 4) words (payload,
-// then the key inputs) | key row (pass 1 with intermediate output) | hist |
+// Shared memory: nr = np + NK fields of (bs + 4) words (payload, then the key
+// inputs; pass 1 of two overwrites the x field with the tile key) | hist |
 // lstart | gbase ([nbcap] each) | bucket starts and batch offsets ([nb1 + 1]
 // each, pass 2) | perm[bs] | sdig[bs] (16-bit).
 template <int DIM, int TILE, int PASS, bool FINAL>
-__global__ void __launch_bounds__(kPartThreads, 1)
-    partition_kernel(KeyGeom g, const float *__restrict__ kx, const float *__restrict__ ky,
-                     const float *__restrict__ kz, long long n, Payload pl, int np,
-                     const unsigned *__restrict__ in_key, unsigned *__restrict__ out_key,
-                     unsigned *__restrict__ gcursor, unsigned tpb, unsigned B,
-                     const unsigned *__restrict__ batch_off, const uint32_t *__restrict__ offs,
-                     unsigned nb1, unsigned nbcap, unsigned bs, unsigned nbatch) {
+__global__ void __launch_bounds__(kPartThreads, 1) partition_kernel(const PartArgs a) {
     extern __shared__ __align__(16) unsigned sm[];
-    __shared__ unsigned warp_tot[kPartThreads / 32];
-    __shared__ BatchGeo s_geo[2];
+    __shared__ __align__(8) uint64_t full[kMaxRows], freeb[kMaxRows];
+    __shared__ BatchGeo s_geo[4];
+    __shared__ unsigned warp_tot[kWorkerWarps];
     constexpr bool kKey = PASS == 1 && !FINAL;
-    constexpr int NK = PASS == 1 ? DIM : 1;  // staged key inputs: positions, or the key
-    const int nl = np + NK;
-    const unsigned row = bs + 4;
-    const size_t buf_words = (size_t)nl * row;  // buffer b starts at sm + b * buf_words
-    unsigned *krow = sm + (size_t)2 * nl * row;
-    unsigned *hist = krow + (kKey ? row : 0u);  // counts, then ranks
-    unsigned *lstart = hist + nbcap;              // local exclusive starts
-    unsigned *gbase = lstart + nbcap;             // reserved global starts
-    unsigned *bstart = gbase + nbcap;             // pass 2: bucket b = [bstart[b], bstart[b+1])
-    unsigned *boff = bstart + (PASS == 2 ? nb1 + 1 : 0u);  // pass 2: first batch of bucket b
-    unsigned short *perm = reinterpret_cast<unsigned short *>(boff + (PASS == 2 ? nb1 + 1 : 0u));
+    constexpr int NK = PASS == 1 ? DIM : 1;  // key fields: positions, or the key
+    const int np = a.np, nr = np + NK;
+    const long long n = a.n;
+    const unsigned bs = a.bs, row = bs + 4;
+    unsigned *hist = sm + (size_t)nr * row;  // counts, then ranks
+    unsigned *lstart = hist + a.nbcap;       // local exclusive starts
+    unsigned *gbase = lstart + a.nbcap;      // reserved global starts
+    unsigned *bstart = gbase + a.nbcap;      // pass 2: bucket b = [bstart[b], bstart[b+1])
+    unsigned *boff = bstart + (PASS == 2 ? a.nb1 + 1 : 0u);  // pass 2: first batch of bucket b
+    unsigned short *perm = reinterpret_cast<unsigned short *>(boff + (PASS == 2 ? a.nb1 + 1 : 0u));
     unsigned short *sdig = perm + bs;
-    const unsigned tid = threadIdx.x;
+    const unsigned tid = threadIdx.x, lane = tid & 31;
 
-    if (PASS == 2) {
-        for (unsigned b = tid; b <= nb1; b += kPartThreads) {
-            const unsigned long long t = (unsigned long long)b * tpb;
-            bstart[b] = t < B ? offs[t] : (unsigned)n;
-            boff[b] = batch_off[b];
+    if (tid == 0) {
+        for (int r = 0; r < nr; ++r) {
+            tc::mbar_init(&full[r], 1);
+            tc::mbar_init(&freeb[r], kWorkerWarps);
         }
-        __syncthreads();
+        fence_mbar_init();
     }
-    auto geometry = [&](unsigned k, BatchGeo &o) {
-        o.len = 0;
-        o.b0 = 0;
-        o.base = 0;
-        o.nb = 1;
-        if (k >= nbatch) return;
-        if (PASS == 1) {
-            o.b0 = (long long)k * bs;
-            const long long rem = n - o.b0;
-            o.len = rem < (long long)bs ? (unsigned)(rem > 0 ? rem : 0) : bs;
-            o.nb = FINAL ? B : nb1;
-        } else {
-            // bucket of batch k: largest b with boff[b] <= k
-            unsigned lo = 0, hi = nb1;
-            while (lo < hi) {
-                const unsigned mid = (lo + hi + 1) / 2;
-                if (boff[mid] <= k) lo = mid;
-                else hi = mid - 1;
-            }
-            if (lo >= nb1) return;
-            o.b0 = (long long)bstart[lo] + (long long)(k - boff[lo]) * bs;
-            const long long rem = (long long)bstart[lo + 1] - o.b0;
-            o.len = rem < (long long)bs ? (unsigned)(rem > 0 ? rem : 0) : bs;
-            o.base = lo * tpb;
-            o.nb = min(tpb, B - o.base);
+    for (unsigned d = tid; d < a.nbcap; d += kPartThreads) hist[d] = 0;
+    if (PASS == 2) {
+        for (unsigned b = tid; b <= a.nb1; b += kPartThreads) {
+            const unsigned long long t = (unsigned long long)b * a.tpb;
+            bstart[b] = t < a.B ? a.offs[t] : (unsigned)n;
+            boff[b] = a.batch_off[b];
         }
-    };
-    auto issue = [&](const BatchGeo &o, unsigned *dst) {
-        if (o.len == 0) return;
-        for (int f = 0; f < np; ++f) stage_field(dst + (size_t)f * row, pl.in[f], o.b0, o.len, n);
-        if (PASS == 1) {
-            stage_field(dst + (size_t)np * row, reinterpret_cast<const unsigned *>(kx), o.b0, o.len, n);
-            stage_field(dst + (size_t)(np + 1) * row, reinterpret_cast<const unsigned *>(ky), o.b0, o.len, n);
-            if (DIM == 3)
-                stage_field(dst + (size_t)(np + 2) * row, reinterpret_cast<const unsigned *>(kz), o.b0,
-                            o.len, n);
-        } else {
-            stage_field(dst + (size_t)np * row, in_key, o.b0, o.len, n);
-        }
-    };
-
-    if (tid == 0) geometry(blockIdx.x, s_geo[0]);
+    }
     __syncthreads();
-    issue(s_geo[0], sm);
-    cp_async_commit();
-    int it = 0;
-    for (unsigned k = blockIdx.x; k < nbatch; k += gridDim.x, ++it) {
-        const int cb = it & 1;
-        if (tid == 0) geometry(k + gridDim.x, s_geo[cb ^ 1]);
-        const BatchGeo cur = s_geo[cb];
-        for (unsigned d = tid; d < cur.nb; d += kPartThreads) hist[d] = 0;
-        __syncthreads();  // next geometry visible, histogram zeroed
-        issue(s_geo[cb ^ 1], sm + (cb ^ 1) * buf_words);
-        cp_async_commit();
-        if (cur.len == 0) break;  // uniform; only trailing batches of pass 2 are empty
-        cp_async_wait_one();      // this thread's copies of the current batch
-        __syncthreads();          // everyone's copies
-        const unsigned *st = sm + cb * buf_words;
+
+    if (tid >= (unsigned)kPartWorkers) {
+        // ---- producer warp ----
+        auto geometry = [&](unsigned k, BatchGeo &o) {
+            o.len = 0;
+            o.b0 = 0;
+            o.base = 0;
+            o.nb = 1;
+            if (k >= a.nbatch) return;
+            if (PASS == 1) {
+                o.b0 = (long long)k * bs;
+                const long long rem = n - o.b0;
+                o.len = rem < (long long)bs ? (unsigned)(rem > 0 ? rem : 0) : bs;
+                o.nb = FINAL ? a.B : a.nb1;
+            } else {
+                // bucket of batch k: largest b with boff[b] <= k
+                unsigned lo = 0, hi = a.nb1;
+                while (lo < hi) {
+                    const unsigned mid = (lo + hi + 1) / 2;
+                    if (boff[mid] <= k) lo = mid;
+                    else hi = mid - 1;
+                }
+                if (lo >= a.nb1) return;
+                o.b0 = (long long)bstart[lo] + (long long)(k - boff[lo]) * bs;
+                const long long rem = (long long)bstart[lo + 1] - o.b0;
+                o.len = rem < (long long)bs ? (unsigned)(rem > 0 ? rem : 0) : bs;
+                o.base = lo * a.tpb;
+                o.nb = min(a.tpb, a.B - o.base);
+            }
+        };
+        auto source = [&](int r) -> const unsigned * {
+            if (r < np) return a.pl.in[r];
+            if (PASS == 2) return a.in_key;
+            const int q = r - np;
+            return reinterpret_cast<const unsigned *>(q == 0 ? a.kx : (q == 1 ? a.ky : a.kz));
+        };
+        // field r of batch o into its staging row: element b0 lands at row[b0 % 4];
+        // one bulk copy from the 16-byte boundary at or below b0 to the one at
+        // or below the end, plain loads for the rest (all of it when the array
+        // is not 16-byte aligned)
+        auto stage = [&](int r, const BatchGeo &o) {
+            const unsigned *src = source(r);
+            unsigned *dst = sm + (size_t)r * row;
+            const long long a0 = o.b0 & ~3ll;
+            const int sh = (int)(o.b0 - a0);
+            const long long e = o.b0 + o.len;
+            const bool al = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+            long long e16 = al ? (e & ~3ll) : a0;
+            if (e16 < a0) e16 = a0;
+            const long long t0 = e16 > o.b0 ? e16 : o.b0;
+            for (long long t = t0 + lane; t < e; t += 32) dst[sh + (t - o.b0)] = src[t];
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t bytes = (uint32_t)(e16 - a0) * 4u;
+                if (bytes) {
+                    mbar_expect_tx(&full[r], bytes);
+                    bulk_g2s(dst, src + a0, bytes, &full[r]);
+                } else {
+                    tc::mbar_arrive(&full[r]);
+                }
+            }
+        };
+        bool ok = true;
+        unsigned k = 0;
+        uint32_t issued = 0;  // fields of batch k already issued (bit r)
+        for (;; ++k) {
+            BatchGeo o;
+            geometry(blockIdx.x + k * gridDim.x, o);
+            if (lane == 0) s_geo[k & 3] = o;
+            issued = 0;
+            // the key fields first: the workers rank with them before they need the payload
+            for (int q = 0; q < nr && ok; ++q) {
+                const int r = q < NK ? np + q : q - NK;
+                if (k > 0) {
+                    // the workers are done with this field of the previous batch
+                    bool w = true;
+                    if (lane == 0) w = tc::mbar_wait_sleep(&freeb[r], (k - 1) & 1, kPartPolls, kPartSleepNs);
+                    ok = __shfl_sync(0xffffffffu, w, 0);
+                    if (!ok) break;
+                }
+                if (o.len == 0) {
+                    // no batch left: complete the key fields' phases so that
+                    // the workers read the empty geometry and leave
+                    if (q < NK) {
+                        if (lane == 0) tc::mbar_arrive(&full[r]);
+                        issued |= 1u << r;
+                    }
+                    continue;
+                }
+                stage(r, o);
+                issued |= 1u << r;
+            }
+            if (!ok || o.len == 0) break;
+        }
+        if (!ok) {
+            // leave only after the copies in flight have landed
+            if (lane == 0) {
+                for (int r = 0; r < nr; ++r) {
+                    if (issued & (1u << r)) (void)tc::mbar_wait_sleep(&full[r], k & 1, kPartPolls, kPartSleepNs);
+                    else if (k > 0) (void)tc::mbar_wait_sleep(&full[r], (k - 1) & 1, kPartPolls, kPartSleepNs);
+                }
+                if (a.flags) atomicOr(a.flags, PCG_FLAG_TIMEOUT);
+            }
+        }
+        return;
+    }
+
+    // ---- worker warps ----
+    bool bad = false;  // this thread gave up a wait
+    for (unsigned k = 0;; ++k) {
+        const uint32_t par = k & 1;
+        for (int q = 0; q < NK; ++q)
+            bad |= !tc::mbar_wait_sleep(&full[np + q], par, kPartPolls, kPartSleepNs);
+        BatchGeo cur = s_geo[k & 3];
+        // (after a timeout the geometry may be stale: keep every index in range
+        // until the workers leave together below)
+        if (cur.len > bs) cur.len = bs;
+        if (cur.nb < 1 || cur.nb > a.nbcap) cur.nb = 1;
         const int sh = (int)(cur.b0 & 3);
+        unsigned *keyrow = sm + (size_t)np * row + sh;
         unsigned dig[kItems], rk[kItems];
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
-            const unsigned i = tid + j * kPartThreads;
+            const unsigned i = tid + j * kPartWorkers;
             dig[j] = 0xffffffffu;
             if (i < cur.len) {
                 unsigned key;
                 if (PASS == 1) {
-                    const float x = __uint_as_float(st[(size_t)np * row + sh + i]);
-                    const float y = __uint_as_float(st[(size_t)(np + 1) * row + sh + i]);
-                    const float z = DIM == 3 ? __uint_as_float(st[(size_t)(np + 2) * row + sh + i]) : 0.f;
-                    key = tile_key<DIM, TILE>(g, x, y, z);
+                    const float x = __uint_as_float(keyrow[i]);
+                    const float y = __uint_as_float(keyrow[row + i]);
+                    const float z = DIM == 3 ? __uint_as_float(keyrow[2 * row + i]) : 0.f;
+                    key = tile_key<DIM, TILE>(a.g, x, y, z);
+                    if (kKey) keyrow[i] = key;  // the x field now holds the key
                 } else {
-                    key = st[(size_t)np * row + sh + i];
+                    key = keyrow[i];
                 }
-                if (kKey) krow[i] = key;
-                unsigned d = (PASS == 1) ? (FINAL ? key : key / tpb) : key - cur.base;
+                unsigned d = (PASS == 1) ? (FINAL ? key : key / a.tpb) : key - cur.base;
                 if (d >= cur.nb) d = cur.nb - 1;  // defensive: never index outside the histogram
                 dig[j] = d;
                 rk[j] = atomicAdd(&hist[d], 1u);
             }
         }
-        __syncthreads();
-        for (unsigned d = tid; d < cur.nb; d += kPartThreads) lstart[d] = hist[d];
-        __syncthreads();
-        block_exclusive_scan(lstart, cur.nb, warp_tot);
-        for (unsigned d = tid; d < cur.nb; d += kPartThreads) {
+        // key fields that are not written out are free for the next batch
+        __syncwarp();
+        if (lane == 0)
+            for (int q = kKey ? 1 : 0; q < NK; ++q) tc::mbar_arrive(&freeb[np + q]);
+        if (work_any(bad || cur.len == 0)) break;  // uniform: done, or a wait gave up
+        work_exclusive_scan(hist, lstart, cur.nb, warp_tot);
+        for (unsigned d = tid; d < cur.nb; d += kPartWorkers) {
             const unsigned c = hist[d];
-            gbase[d] = c ? atomicAdd(&gcursor[cur.base + d], c) : 0u;
+            gbase[d] = c ? atomicAdd(&a.gcursor[cur.base + d], c) : 0u;
+            hist[d] = 0;  // ready for the next batch
         }
 #pragma unroll
         for (int j = 0; j < kItems; ++j) {
             if (dig[j] == 0xffffffffu) continue;
             const unsigned slot = lstart[dig[j]] + rk[j];
-            perm[slot] = (unsigned short)(tid + j * kPartThreads);
+            perm[slot] = (unsigned short)(tid + j * kPartWorkers);
             sdig[slot] = (unsigned short)dig[j];
         }
-        __syncthreads();
-        // write every digit's run with consecutive threads; all of a slot's
-        // shared-memory loads are issued before its stores
-        for (unsigned slot = tid; slot < cur.len; slot += kPartThreads) {
-            const unsigned i = perm[slot], d = sdig[slot];
-            const unsigned gpos = gbase[d] + (slot - lstart[d]);
-            if (!PCG_IN(gpos, n) || !PCG_IN(i, cur.len)) continue;
-            const unsigned *src = st + sh + i;
-            if (PASS == 2) {
-                // measured faster for pass 2: one load-store pair per field
-                for (int f = 0; f < np; ++f) pl.out[f][gpos] = src[(size_t)f * row];
-            } else {
-                // measured faster for pass 1: all loads of the slot before its stores
-                unsigned v[kMaxPayload];
+        work_sync();
+        // this thread's output slots: source row and global position
+        unsigned src[kItems], gpos[kItems];
 #pragma unroll
-                for (int f = 0; f < kMaxPayload; ++f)
-                    if (f < np) v[f] = src[(size_t)f * row];
-                const unsigned kv = kKey ? krow[i] : 0u;
-#pragma unroll
-                for (int f = 0; f < kMaxPayload; ++f)
-                    if (f < np) pl.out[f][gpos] = v[f];
-                if (kKey) out_key[gpos] = kv;
+        for (int j = 0; j < kItems; ++j) {
+            const unsigned s = tid + j * kPartWorkers;
+            src[j] = 0xffffffffu;
+            if (s < cur.len) {
+                const unsigned i = perm[s], d = sdig[s];
+                const unsigned gp = gbase[d] + (s - lstart[d]);
+                if (PCG_IN(gp, n) && (long long)gp < n && PCG_IN(i, cur.len)) {
+                    src[j] = i;
+                    gpos[j] = gp;
+                }
             }
         }
-        __syncthreads();  // buffer, key row, histogram and permutation are reused
+        // write every digit's run with consecutive threads, field by field,
+        // releasing each field to the producer as soon as this warp is done
+        if (kKey) {
+#pragma unroll
+            for (int j = 0; j < kItems; ++j)
+                if (src[j] != 0xffffffffu) a.out_key[gpos[j]] = keyrow[src[j]];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&freeb[np]);
+        }
+        for (int f = 0; f < np; ++f) {
+            bad |= !tc::mbar_wait_sleep(&full[f], par, kPartPolls, kPartSleepNs);
+            const unsigned *fr = sm + (size_t)f * row + sh;
+            unsigned *out = a.pl.out[f];
+#pragma unroll
+            for (int j = 0; j < kItems; ++j)
+                if (src[j] != 0xffffffffu) out[gpos[j]] = fr[src[j]];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&freeb[f]);
+        }
     }
-    cp_async_wait_all();
+    if (bad && a.flags) atomicOr(a.flags, PCG_FLAG_TIMEOUT);
 }
 
 size_t partition_smem(int DIM, int pass, bool final_, int np, unsigned nbcap, unsigned nb1, unsigned bs) {
     const int nk = pass == 1 ? DIM : 1;
     const size_t row = (size_t)(bs + 4) * 4;
-    size_t b = 2 * (size_t)(np + nk) * row;
-    if (pass == 1 && !final_) b += row;
+    size_t b = (size_t)(np + nk) * row;
     b += (size_t)3 * nbcap * 4;
     if (pass == 2) b += (size_t)2 * (nb1 + 1) * 4;
     b += (size_t)bs * 4;  // perm + sdig
     return b;
 }
 
-// Largest batch (<= kMaxBatch, a multiple of kPartThreads) whose buffers fit.
+// Largest batch (<= kMaxBatch, a multiple of kPartWorkers) whose buffers fit.
 unsigned partition_batch(int DIM, int pass, bool final_, int np, unsigned nbcap, unsigned nb1) {
-    constexpr size_t kSmemCap = 227 * 1024 - 1024;
-    for (unsigned bs = kMaxBatch; bs > (unsigned)kPartThreads; bs /= 2)
+    constexpr size_t kSmemCap = 227 * 1024 - 1024;  // less the static shared memory
+    for (unsigned bs = kMaxBatch; bs > (unsigned)kPartWorkers; bs /= 2)
         if (partition_smem(DIM, pass, final_, np, nbcap, nb1, bs) <= kSmemCap) return bs;
-    return kPartThreads;
+    return kPartWorkers;
 }
 
 // cursor1[b] = start of bucket b; cursor2[t] = start of tile t (written by the
@@ -552,6 +650,8 @@ struct Plan {
     unsigned G;        // chunks (chunked path and the chunked count of the two-pass path)
     long long chunk;   // particles per chunk
     unsigned tpb, nb1; // two-pass: tiles per bucket, buckets (1 = single pass)
+    unsigned bs1, bs2; // two-pass: batch rows of pass 1 and pass 2
+    size_t smem1, smem2;
     size_t bytes;      // workspace bytes
     size_t smem;       // dynamic shared memory of the chunked count / scatter
     // workspace layout (byte offsets)
@@ -566,7 +666,7 @@ struct Plan {
 // read-modify-write on every sector, so the two-pass partition is used.
 constexpr double kL2Resident = 96.0 * 1024 * 1024;
 
-Plan make_plan(const TileGrid &tg, long long n, int n_payload) {
+Plan make_plan(const TileGrid &tg, long long n, int n_payload, int dim) {
     Plan p{};
     p.B = (unsigned)(tg.n_tiles + 1);
     const double out = (double)n * n_payload * 4.0;
@@ -596,6 +696,16 @@ Plan make_plan(const TileGrid &tg, long long n, int n_payload) {
         p.G = (unsigned)G;
         p.chunk = align_up((size_t)((n + G - 1) / G), 4);  // chunks start 16-byte aligned
         if (p.chunk < 4) p.chunk = 4;
+    }
+    if (p.path == kTwoPass) {
+        const bool fin = p.nb1 == 1;
+        const unsigned cap1 = fin ? p.B : p.nb1;
+        p.bs1 = partition_batch(dim, 1, fin, n_payload, cap1, p.nb1);
+        p.smem1 = partition_smem(dim, 1, fin, n_payload, cap1, p.nb1, p.bs1);
+        if (!fin) {
+            p.bs2 = partition_batch(dim, 2, false, n_payload, p.tpb, p.nb1);
+            p.smem2 = partition_smem(dim, 2, false, n_payload, p.tpb, p.nb1, p.bs2);
+        }
     }
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -700,57 +810,70 @@ pcg_status run_sort(const TileGrid &tg, const Plan &pl, long long n, const float
         return launch_status();
     }
     const unsigned sms = (unsigned)num_sms();
-    // two-pass partition with global cursors: one persistent CTA per SM
+    PartArgs a{};
+    a.g = g;
+    a.kx = kp[0];
+    a.ky = kp[1];
+    a.kz = kz;
+    a.n = n;
+    a.np = np;
+    a.offs = offs;
+    a.flags = flags;
+    a.B = pl.B;
+    a.nb1 = pl.nb1;
+    a.tpb = pl.tpb;
     if (pl.nb1 == 1) {
-        const unsigned bs = partition_batch(DIM, 1, true, np, pl.B, 1);
-        const size_t smem = partition_smem(DIM, 1, true, np, pl.B, 1, bs);
-        const unsigned nbatch = (unsigned)((n + bs - 1) / bs);
-        PCG_CHECK_CUDA(cudaFuncSetAttribute(partition_kernel<DIM, TILE, 1, true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        // one pass: the digits are the tiles
+        auto kern = partition_kernel<DIM, TILE, 1, true>;
+        PCG_CHECK_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem1));
+        a.pl = py;
+        a.gcursor = cursor;
+        a.nbcap = pl.B;
+        a.bs = pl.bs1;
+        a.nbatch = (unsigned)((n + pl.bs1 - 1) / pl.bs1);
         prof::Mark mk("sort_partition", s);
-        partition_kernel<DIM, TILE, 1, true><<<nbatch < sms ? nbatch : sms, kPartThreads, smem, s>>>(
-            g, kp[0], kp[1], kz, n, py, np, nullptr, nullptr, cursor, 1, pl.B, nullptr, offs, 1, pl.B, bs,
-            nbatch);
+        kern<<<min(a.nbatch, sms), kPartThreads, pl.smem1, s>>>(a);
         return launch_status();
     }
     unsigned *cursor1 = reinterpret_cast<unsigned *>(ws + pl.o_cursor1);
     unsigned *batch = reinterpret_cast<unsigned *>(ws + pl.o_batch);
     unsigned *ikey = reinterpret_cast<unsigned *>(ws + pl.o_key);
-    Payload p1{}, p2{};
+    PartArgs a1 = a, a2 = a;
     for (int f = 0; f < np; ++f) {
         unsigned *inter = reinterpret_cast<unsigned *>(ws + pl.o_inter + (size_t)f * pl.inter_stride);
-        p1.in[f] = py.in[f];
-        p1.out[f] = inter;
-        p2.in[f] = inter;
-        p2.out[f] = py.out[f];
+        a1.pl.in[f] = py.in[f];
+        a1.pl.out[f] = inter;
+        a2.pl.in[f] = inter;
+        a2.pl.out[f] = py.out[f];
     }
-    const unsigned bs1 = partition_batch(DIM, 1, false, np, pl.nb1, pl.nb1);
-    const unsigned bs2 = partition_batch(DIM, 2, false, np, pl.tpb, pl.nb1);
-    const size_t smem1 = partition_smem(DIM, 1, false, np, pl.nb1, pl.nb1, bs1);
-    const size_t smem2 = partition_smem(DIM, 2, false, np, pl.tpb, pl.nb1, bs2);
+    a1.out_key = ikey;
+    a1.gcursor = cursor1;
+    a1.nbcap = pl.nb1;
+    a1.bs = pl.bs1;
+    a1.nbatch = (unsigned)((n + pl.bs1 - 1) / pl.bs1);
+    a2.in_key = ikey;
+    a2.gcursor = cursor;
+    a2.batch_off = batch;
+    a2.nbcap = pl.tpb;
+    a2.bs = pl.bs2;
+    // upper bound on the bucket-aligned batches; the ones past the real count are empty
+    a2.nbatch = (unsigned)((n + pl.bs2 - 1) / pl.bs2) + pl.nb1;
     {
         prof::Mark mk("sort_bucket_setup", s);
-        bucket_setup_kernel<<<1, 1024, 0, s>>>(offs, n, pl.B, pl.tpb, pl.nb1, bs2, cursor1, batch);
+        bucket_setup_kernel<<<1, 1024, 0, s>>>(offs, n, pl.B, pl.tpb, pl.nb1, pl.bs2, cursor1, batch);
     }
     PCG_CHECK_LAUNCH();
-    PCG_CHECK_CUDA(cudaFuncSetAttribute(partition_kernel<DIM, TILE, 1, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1));
-    PCG_CHECK_CUDA(cudaFuncSetAttribute(partition_kernel<DIM, TILE, 2, false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2));
-    const unsigned nbatch1 = (unsigned)((n + bs1 - 1) / bs1);
+    auto k1 = partition_kernel<DIM, TILE, 1, false>;
+    auto k2 = partition_kernel<DIM, TILE, 2, false>;
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem1));
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem2));
     {
         prof::Mark mk("sort_partition1", s);
-        partition_kernel<DIM, TILE, 1, false><<<nbatch1 < sms ? nbatch1 : sms, kPartThreads, smem1, s>>>(
-            g, kp[0], kp[1], kz, n, p1, np, nullptr, ikey, cursor1, pl.tpb, pl.B, batch, offs, pl.nb1,
-            pl.nb1, bs1, nbatch1);
+        k1<<<min(a1.nbatch, sms), kPartThreads, pl.smem1, s>>>(a1);
     }
     PCG_CHECK_LAUNCH();
-    // upper bound on the bucket-aligned batches; the ones past the real count are empty
-    const unsigned nbatch2 = (unsigned)((n + bs2 - 1) / bs2) + pl.nb1;
     prof::Mark mk("sort_partition2", s);
-    partition_kernel<DIM, TILE, 2, false><<<nbatch2 < sms ? nbatch2 : sms, kPartThreads, smem2, s>>>(
-        g, kp[0], kp[1], kz, n, p2, np, ikey, nullptr, cursor, pl.tpb, pl.B, batch, offs, pl.nb1, pl.tpb,
-        bs2, nbatch2);
+    k2<<<min(a2.nbatch, sms), kPartThreads, pl.smem2, s>>>(a2);
     return launch_status();
 }
 
@@ -781,7 +904,7 @@ extern "C" pcg_status pcg_tile_sort_workspace_size(int32_t dim, const int32_t *g
     TileGrid tg;
     if (bytes == nullptr || !valid_sort_args(dim, grid, tile, n, &tg)) return PCG_ERR_INVALID_ARG;
     if (n_payload < 1 || n_payload > kMaxPayload) return PCG_ERR_INVALID_ARG;
-    *bytes = make_plan(tg, n, n_payload).bytes;
+    *bytes = make_plan(tg, n, n_payload, dim).bytes;
     return PCG_OK;
 }
 
@@ -805,7 +928,7 @@ extern "C" pcg_status pcg_tile_sort(int32_t dim, const int32_t *grid, int32_t ti
     }
     for (int mu = 0; mu < dim; ++mu)
         if (n > 0 && key_pos[mu] == nullptr) return PCG_ERR_INVALID_ARG;
-    const Plan pl = make_plan(tg, n, n_payload);
+    const Plan pl = make_plan(tg, n, n_payload, dim);
     if (workspace_bytes < pl.bytes || (pl.bytes > 0 && workspace == nullptr))
         return PCG_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return PCG_ERR_WORKSPACE;

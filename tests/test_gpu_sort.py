@@ -89,3 +89,18 @@ def test_sort_skewed_density():
     pos = [rng.uniform(0, 8, n).astype(np.float32) for _ in range(3)]
     pos[0][:10] = rng.uniform(8, 64, 10).astype(np.float32)
     _check_sort(pcg, (64, 64, 64), 8, pos)
+
+
+@pytest.mark.parametrize("grid,tile", [((128, 128, 128), 4), ((64, 64, 64), 8)])
+def test_sort_partition_skewed(grid, tile):
+    # partition sizes with 90% of the particles in one tile: the bucket (and,
+    # in one pass, the tile) that holds them spans many chunks of the count
+    pcg = need_gpu()
+    rng = np.random.default_rng(11)
+    n = 9_000_003
+    pos = _particles(rng, grid, n, invalid=17)
+    hot = rng.random(n) < 0.9
+    for mu in range(3):
+        pos[mu][hot] = rng.uniform(tile, 2 * tile, int(hot.sum())).astype(np.float32)
+    _check_sort(pcg, grid, tile, pos)
+
