@@ -315,25 +315,32 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
 
     if e2e_steps:
         # end to end through the public API: every step copies its inputs from
-        # pinned host memory to the device and reads J back.  The copies of step
-        # k + 1 run on a second stream into a second set of device inputs while
-        # step k computes (what a production loop does); both sets alternate.
+        # pinned host memory to the device and reads J back.  Three streams: the
+        # copies of step k + 1's inputs run on an upload stream into a second set
+        # of device inputs while step k computes; J alternates between two
+        # device buffers and each step's J is read back on a third stream, so
+        # that the compute stream never queues behind a copy (it waits only for
+        # its inputs and for the read-back of the J buffer it is about to reuse).
         h_in = [torch.from_numpy(a).pin_memory() for a in (list(d["key_pos"]) if separate_keys else [])
                 + list(d["pos"]) + list(d["vel"]) + [d["q"]]]
         sets = [(kp if separate_keys else []) + payload]
         sets.append([torch.empty_like(t) for t in sets[0]])
-        h_J = torch.empty(J.shape, dtype=torch.float32).pin_memory()
+        Jb = [J, torch.empty_like(J)]
+        h_J = [torch.empty(J.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
         nk = dim if separate_keys else 0
-        cs = torch.cuda.Stream()
-        ready = [torch.cuda.Event(), torch.cuda.Event()]
-        free = [torch.cuda.Event(), torch.cuda.Event()]
+        cs = torch.cuda.Stream()   # uploads
+        rs = torch.cuda.Stream()   # read-backs
+        ready = [torch.cuda.Event(), torch.cuda.Event()]   # inputs of set b on the device
+        free = [torch.cuda.Event(), torch.cuda.Event()]    # set b consumed by its step
+        done = [torch.cuda.Event(), torch.cuda.Event()]    # J buffer b written by its step
+        read = [torch.cuda.Event(), torch.cuda.Event()]    # J buffer b read back
 
-        def step_on(dset):
+        def step_on(dset, Jt):
             kpp = dset[:nk] if separate_keys else dset[:dim]
             py = dset[nk:]
             pcg.tile_sort(grid, d["tile"], kpp, py, out=out, tile_offsets=offs, workspace=ws_s)
             pcg.deposit_current(grid, d["order"], out[:dim], out[dim:dim + 3], out[dim + 3], tile_offsets=offs,
-                                tile=d["tile"], halo=d["halo"], J=J, stats=stats, workspace=ws_d)
+                                tile=d["tile"], halo=d["halo"], J=Jt, stats=stats, workspace=ws_d)
 
         def upload(b):
             with torch.cuda.stream(cs):
@@ -344,7 +351,9 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
         def e2e_run(k_steps):
             for b in (0, 1):
                 free[b].record(stream)
+                read[b].record(stream)
             cs.wait_stream(stream)
+            rs.wait_stream(stream)
             upload(0)
             for k in range(k_steps):
                 b = k & 1
@@ -352,9 +361,15 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
                     cs.wait_event(free[b ^ 1])
                     upload(b ^ 1)
                 stream.wait_event(ready[b])
-                step_on(sets[b])
+                stream.wait_event(read[b])
+                step_on(sets[b], Jb[b])
                 free[b].record(stream)
-                h_J.copy_(J, non_blocking=True)
+                done[b].record(stream)
+                rs.wait_event(done[b])
+                with torch.cuda.stream(rs):
+                    h_J[b].copy_(Jb[b], non_blocking=True)
+                    read[b].record(rs)
+            stream.wait_stream(rs)
 
         e2e_run(2)  # warm-up
         torch.cuda.synchronize()
@@ -372,7 +387,8 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
         res["e2e"] = {"value": round(n * e2e_steps * dist.world / (ms_e * 1e-3) / 1e6, 3), "unit": UNIT,
                       "h2d_bytes_per_step": int(sum(h.numel() * 4 for h in h_in)),
                       "d2h_bytes_per_step": int(J.numel() * 4), "ms_per_step": round(ms_e / e2e_steps, 3),
-                      "overlap": "inputs of step k+1 copied on a second stream during step k"}
+                      "overlap": "inputs of step k+1 uploaded on a second stream during step k; J double-buffered "
+                                 "and read back on a third stream"}
         # the host link alone: the same pinned copies with nothing else running
         la = torch.cuda.Event(enable_timing=True)
         lb = torch.cuda.Event(enable_timing=True)
@@ -383,7 +399,7 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
         lb.record(cs)
         torch.cuda.synchronize()
         res["e2e"]["h2d_alone_gbs"] = round(res["e2e"]["h2d_bytes_per_step"] / (la.elapsed_time(lb) * 1e-3) / 1e9, 1)
-        del h_in, h_J, sets
+        del h_in, h_J, sets, Jb
     del pos, vel, q, kp, payload, out, J, ws_s, ws_d
     torch.cuda.empty_cache()
     return res
