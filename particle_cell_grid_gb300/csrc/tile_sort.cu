@@ -252,6 +252,12 @@ constexpr int kWorkerWarps = kPartWorkers / 32;
 constexpr int kMaxBatch = 4096;
 constexpr int kItems = kMaxBatch / kPartWorkers;
 constexpr unsigned kMaxPassBins = 2048;
+// Pass-1 buckets.  A batch's runs are about bs / digits rows long and the
+// store phase costs about the same per run, so the two passes' digit counts
+// are balanced: 128 buckets (257 tiles each at 256^3 / 8) measured best among
+// 96, 128, 160, 181 and 256 (pass 1 writes one field more than pass 2).  Up to
+// kMaxBuckets when the tiles per bucket would exceed kMaxPassBins.
+constexpr unsigned kBuckets = 128;
 constexpr unsigned kMaxBuckets = 256;
 constexpr int kMaxRows = kMaxPayload + 3;
 constexpr uint32_t kPartPolls = 1u << 20;  // bounded waits: about 1 s with the 1 us suspend hint
@@ -678,7 +684,8 @@ Plan make_plan(const TileGrid &tg, long long n, int n_payload, int dim) {
             p.nb1 = 1;
             p.tpb = p.B;
         } else {
-            p.tpb = (p.B + kMaxBuckets - 1) / kMaxBuckets;
+            p.tpb = (p.B + kBuckets - 1) / kBuckets;
+            if (p.tpb > kMaxPassBins) p.tpb = (p.B + kMaxBuckets - 1) / kMaxBuckets;
             if (p.tpb > kMaxPassBins) p.path = kGlobal;  // too many bins for two passes
             p.nb1 = (p.B + p.tpb - 1) / p.tpb;
         }
