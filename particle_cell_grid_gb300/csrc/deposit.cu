@@ -70,6 +70,19 @@ long long chunk_for(long long n) {
     return c;
 }
 
+// The 3D quadratic kernel flushes its window of 11^3 nodes at every tile
+// segment end, so it takes larger chunks (fewer segments split across chunks);
+// never smaller than chunk_for(n), so the workspace sized by chunk_for holds
+// its chunk map.
+constexpr long long kQuadChunkMax = 65536;
+long long chunk_for_shape(long long n, int dim, int order, int tile, bool tiled) {
+    long long c = chunk_for(n);
+    if (!(tiled && dim == 3 && order == 2 && tile == 8)) return c;
+    const long long target = n / ((long long)num_sms() * 8);
+    while (c < target && c < kQuadChunkMax) c <<= 1;
+    return c;
+}
+
 bool geom_from(int32_t dim, const int32_t *grid, int tile, Geom *g) {
     TileGrid tg;
     if (!make_tile_grid(dim, grid, tile < 1 ? 1 : tile, &tg)) return false;
@@ -154,7 +167,7 @@ extern "C" pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int3
         const pcg_status st = check_current_args(dim, grid, order, tile, halo, block, n, pos, vel, q, tiled, J, &g);
         if (st != PCG_OK) return st;
     }
-    const long long chunk = chunk_for(n);
+    const long long chunk = chunk_for_shape(n, dim, order, tile, tiled);
     const long long nchunks = (n + chunk - 1) / chunk;
     const size_t need = tiled ? align_up((size_t)nchunks * sizeof(unsigned), 256) : 0;
     if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return PCG_ERR_WORKSPACE;
@@ -260,7 +273,7 @@ extern "C" pcg_status pcg_deposit_current_noalloc(int32_t dim, const int32_t *gr
                                                  tile_offsets != nullptr, J, &g);
         if (st != PCG_OK) return st;
     }
-    const long long chunk = chunk_for(n);
+    const long long chunk = chunk_for_shape(n, dim, order, tile, tile_offsets != nullptr);
     const long long nchunks = (n + chunk - 1) / chunk;
     if (tile_offsets != nullptr && (size_t)nchunks > kNoAllocChunks) return PCG_ERR_WORKSPACE;
     unsigned *scratch = nullptr;

@@ -917,6 +917,14 @@ pcg_status launch_cic3d_v5(const Geom &g, long long n, const Particles &P, const
 }
 
 
+}  // namespace dep
+}  // namespace pcg
+
+#include "deposit_quad3d.cuh"
+
+namespace pcg {
+namespace dep {
+
 template <int DIM, int ORDER, int TILE, int HALO, int THREADS>
 size_t tiled_smem() {
     using C = TileCfg<DIM, ORDER, TILE, HALO>;
@@ -947,6 +955,8 @@ pcg_status launch_tiled(const Geom &g, long long n, const Particles &P, const ui
     if constexpr (DIM == 3 && ORDER == 1 && TILE == 8) {
         // block 512 asks for one 512-thread CTA per SM with the full register file
         return launch_cic3d_v5<HALO>(g, n, P, offs, J, ctr, chunk_tile, chunk, s);
+    } else if constexpr (DIM == 3 && ORDER == 2 && TILE == 8) {
+        return launch_quad3d<HALO>(g, n, P, offs, J, ctr, chunk_tile, chunk, s);
     } else {
         if (block == 512)
             return launch_tiled_t<DIM, ORDER, TILE, HALO, 512>(g, n, P, offs, J, ctr, chunk_tile, chunk, s);

@@ -52,7 +52,7 @@ def test_flat(grid, order):
 
 @pytest.mark.parametrize("grid,tile", [((64, 64), 8), ((37, 21), 8), ((20, 20), 4), ((32, 32, 32), 8),
                                        ((19, 13, 11), 4), ((24, 17, 9), 8)])
-@pytest.mark.parametrize("order,halo", [(1, 0), (1, 1), (1, 2), (2, 1), (2, 2)])
+@pytest.mark.parametrize("order,halo", [(1, 0), (1, 1), (1, 2), (2, 0), (2, 1), (2, 2)])
 def test_tiled_any_halo(grid, tile, order, halo):
     pcg = need_gpu()
     rng = np.random.default_rng(hash((grid, tile, order, halo)) % 2 ** 32)
@@ -84,6 +84,26 @@ def test_tiled_drift_and_escape(order):
     Jr, _ = oracle.deposit_current(grid, order, pos, vel, q)
     assert_deposit_close(J, Jr)
     assert st["n_escaped"] > 0
+
+
+@pytest.mark.parametrize("order", [1, 2])
+def test_tiled_one_dense_cell(order):
+    # ~3500 particles in one cell (about half of each round of that tile): its
+    # support group overflows the per-round lists and the excess takes the
+    # general path.  (Many more in one cell would put the fp32 sum of the
+    # node's contributions, in any order, beyond the 1e-5 relative tolerance.)
+    pcg = need_gpu()
+    grid = (32, 24, 16)
+    rng = np.random.default_rng(19 + order)
+    n = 70001
+    pos, vel, q = _random(rng, grid, n)
+    hot = rng.random(n) < 0.05
+    for mu, c in enumerate((13, 6, 9)):
+        pos[mu][hot] = (c + rng.random(int(hot.sum()))).astype(np.float32)
+    J, st = _deposit(pcg, grid, order, pos, vel, q, tile=8, halo=2)
+    Jr, _ = oracle.deposit_current(grid, order, pos, vel, q)
+    assert_deposit_close(J, Jr)
+    assert st["n_escaped"] == 0 and st["n_invalid"] == 0
 
 
 def test_tiled_stale_layout_unsorted_input():
