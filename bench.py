@@ -73,10 +73,11 @@ def load_traffic():
 
 
 # The source files each timed kernel is built from (all of them for a name not listed).
-_COMMON = ["common.cuh", "profile.cuh"]
+_COMMON = ["common.cuh", "checked.cuh", "profile.cuh"]
 KERNEL_SOURCES = {
-    "sort": ["tile_sort.cu"] + _COMMON,
-    "deposit_tiled": ["deposit_tiled.cuh", "deposit.cuh", "deposit_2d.cu", "deposit_3d.cu"] + _COMMON,
+    "sort": ["tile_sort.cu", "tcgen05.cuh"] + _COMMON,
+    "deposit_tiled": ["deposit_tiled.cuh", "deposit_quad3d.cuh", "deposit.cuh", "deposit.cu", "deposit_2d.cu",
+                      "deposit_3d.cu"] + _COMMON,
     "deposit_zigzag": ["deposit_zigzag.cu", "deposit_tiled.cuh", "deposit.cuh"] + _COMMON,
     "mass": ["mass_matrix.cu", "mass_cic.cuh", "mass_cic_tc.cu", "mass_tsc.cu", "mass_tsc.cuh", "mass_tsc_tc.cu",
              "mass_common.cuh", "tcgen05.cuh"] + _COMMON,

@@ -235,11 +235,13 @@ PCG_API pcg_status pcg_deposit_current(int32_t dim, const int32_t *grid, int32_t
  * pcg_deposit_current, which it calls with its own scratch.
  *
  * Arguments, outputs, stats and errors are those of pcg_deposit_current minus
- * the workspace.  The tiled path's scratch (one 32-bit entry per chunk of up
- * to 16384 particles) is a fixed 256 KB device array inside the library, held
- * on every GPU that loads it until the process exits; so this entry point
- * accepts at most 65536 chunks, i.e. n <= 2^30 particles when tile_offsets is
- * given, and returns PCG_ERR_WORKSPACE above that (before launching anything).
+ * the workspace.  The tiled path's scratch (one 32-bit entry per chunk of
+ * particles) is a fixed 256 KB device array inside the library, held on every
+ * GPU that loads it until the process exits; so this entry point accepts at
+ * most 65536 chunks when tile_offsets is given, and returns PCG_ERR_WORKSPACE
+ * above that (before launching anything).  Chunks hold up to 16384 particles
+ * (up to 65536 for the 3D quadratic deposit on 8^3 tiles), so every
+ * n <= 2^30 fits.
  * The flat path (tile_offsets NULL) uses no scratch and has no such limit.
  *
  * Arguments are checked exactly as pcg_deposit_current checks them, before the

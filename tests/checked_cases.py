@@ -56,6 +56,21 @@ def main():
         J = pcg.deposit_current(g, order, out[:2], out[2:5], out[5], tile_offsets=offs, tile=8, halo=1 + order - 1)
         assert_deposit_close(host(J), Jr, where=f"2D order {order}")
         cases.append(f"deposit 2D order {order}")
+    # the sort's other paths: global counters (more bins than shared memory
+    # holds) and the partition (outputs above 96 MB: 7 M x 4 fields), one pass
+    # and two
+    rng = np.random.default_rng(5)
+    for grid, tile, n in (((64, 64, 64), 1, 40000), ((64, 64, 64), 8, 7_000_001), ((128, 128, 128), 4, 7_000_001)):
+        pos = [rng.uniform(0, N, n).astype(np.float32) for N in grid]
+        ids = np.arange(n, dtype=np.int32)
+        out, offs = pcg.tile_sort(grid, tile, [dev(p) for p in pos], [dev(p) for p in pos] + [dev(ids)])
+        keys, want = oracle.tile_keys(grid, tile, pos)
+        assert np.array_equal(host(offs).astype(np.uint32), want), f"sort offsets {grid} t{tile}"
+        oid = host(out[-1]).astype(np.int64)
+        assert np.array_equal(np.sort(oid), ids), f"sort permutation {grid} t{tile}"
+        slot_tile = np.searchsorted(want, np.arange(n), side="right") - 1
+        assert np.array_equal(keys[oid], slot_tile.astype(np.uint32)), f"sort tiles {grid} t{tile}"
+        cases.append(f"sort {grid} t{tile} n={n}")
     # the zigzag deposit, flat and tiled
     d = synth.zigzag3d(grid=(16, 12, 20), ppc=4, sigma_v=0.3)
     g = d["grid"]

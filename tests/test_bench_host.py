@@ -19,8 +19,9 @@ def _tree(tmp_path, files):
 
 
 def test_kernel_hashes_cover_their_own_sources(tmp_path, monkeypatch):
-    files = {n: n for n in ("tile_sort.cu", "common.cuh", "profile.cuh", "deposit_tiled.cuh", "deposit.cuh",
-                            "deposit_2d.cu", "deposit_3d.cu", "cic1d.cu")}
+    files = {n: n for n in ("tile_sort.cu", "tcgen05.cuh", "common.cuh", "checked.cuh", "profile.cuh",
+                            "deposit_tiled.cuh", "deposit_quad3d.cuh", "deposit.cuh", "deposit.cu", "deposit_2d.cu",
+                            "deposit_3d.cu", "cic1d.cu")}
     csrc = _tree(tmp_path, files)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     sort_h, dep_h = bench.source_hash("sort_partition1"), bench.source_hash("deposit_tiled")
@@ -35,8 +36,9 @@ def test_kernel_hashes_cover_their_own_sources(tmp_path, monkeypatch):
 
 
 def test_stale_traffic_entries_are_ignored(tmp_path, monkeypatch):
-    files = {n: n for n in ("tile_sort.cu", "common.cuh", "profile.cuh", "deposit_tiled.cuh", "deposit.cuh",
-                            "deposit_2d.cu", "deposit_3d.cu")}
+    files = {n: n for n in ("tile_sort.cu", "tcgen05.cuh", "common.cuh", "checked.cuh", "profile.cuh",
+                            "deposit_tiled.cuh", "deposit_quad3d.cuh", "deposit.cuh", "deposit.cu", "deposit_2d.cu",
+                            "deposit_3d.cu")}
     _tree(tmp_path, files)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     lines = [
