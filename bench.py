@@ -72,6 +72,9 @@ def load_traffic():
     return out
 
 
+# Host -> device copies of the end-to-end leg run on this many streams.
+UPLOAD_STREAMS = 4
+
 # The source files each timed kernel is built from (all of them for a name not listed).
 _COMMON = ["common.cuh", "checked.cuh", "profile.cuh"]
 KERNEL_SOURCES = {
@@ -316,10 +319,11 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
 
     if e2e_steps:
         # end to end through the public API: every step copies its inputs from
-        # pinned host memory to the device and reads J back.  Three streams: the
-        # copies of step k + 1's inputs run on an upload stream into a second set
-        # of device inputs while step k computes; J alternates between two
-        # device buffers and each step's J is read back on a third stream, so
+        # pinned host memory to the device and reads J back.  The copies of step
+        # k + 1's inputs run on UPLOAD_STREAMS upload streams (the fields dealt
+        # round-robin, so that several copy engines share the host link) into a
+        # second set of device inputs while step k computes; J alternates between
+        # two device buffers and each step's J is read back on its own stream, so
         # that the compute stream never queues behind a copy (it waits only for
         # its inputs and for the read-back of the J buffer it is about to reuse).
         h_in = [torch.from_numpy(a).pin_memory() for a in (list(d["key_pos"]) if separate_keys else [])
@@ -329,9 +333,9 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
         Jb = [J, torch.empty_like(J)]
         h_J = [torch.empty(J.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
         nk = dim if separate_keys else 0
-        cs = torch.cuda.Stream()   # uploads
+        ups = [torch.cuda.Stream() for _ in range(UPLOAD_STREAMS)]  # uploads
         rs = torch.cuda.Stream()   # read-backs
-        ready = [torch.cuda.Event(), torch.cuda.Event()]   # inputs of set b on the device
+        ready = [[torch.cuda.Event() for _ in ups] for _ in range(2)]  # inputs of set b on the device
         free = [torch.cuda.Event(), torch.cuda.Event()]    # set b consumed by its step
         done = [torch.cuda.Event(), torch.cuda.Event()]    # J buffer b written by its step
         read = [torch.cuda.Event(), torch.cuda.Event()]    # J buffer b read back
@@ -343,25 +347,29 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
             pcg.deposit_current(grid, d["order"], out[:dim], out[dim:dim + 3], out[dim + 3], tile_offsets=offs,
                                 tile=d["tile"], halo=d["halo"], J=Jt, stats=stats, workspace=ws_d)
 
-        def upload(b):
-            with torch.cuda.stream(cs):
-                for h, t in zip(h_in, sets[b]):
-                    t.copy_(h, non_blocking=True)
-                ready[b].record(cs)
+        def upload(b, wait=None):
+            for u, cs in enumerate(ups):
+                if wait is not None:
+                    cs.wait_event(wait)
+                with torch.cuda.stream(cs):
+                    for f in range(u, len(h_in), len(ups)):
+                        sets[b][f].copy_(h_in[f], non_blocking=True)
+                    ready[b][u].record(cs)
 
         def e2e_run(k_steps):
             for b in (0, 1):
                 free[b].record(stream)
                 read[b].record(stream)
-            cs.wait_stream(stream)
+            for cs in ups:
+                cs.wait_stream(stream)
             rs.wait_stream(stream)
             upload(0)
             for k in range(k_steps):
                 b = k & 1
                 if k + 1 < k_steps:
-                    cs.wait_event(free[b ^ 1])
-                    upload(b ^ 1)
-                stream.wait_event(ready[b])
+                    upload(b ^ 1, wait=free[b ^ 1])
+                for ev in ready[b]:
+                    stream.wait_event(ev)
                 stream.wait_event(read[b])
                 step_on(sets[b], Jb[b])
                 free[b].record(stream)
@@ -388,18 +396,32 @@ def current_workload(pcg, d, steps, warmup, dist, peaks, traffic, e2e_steps=0):
         res["e2e"] = {"value": round(n * e2e_steps * dist.world / (ms_e * 1e-3) / 1e6, 3), "unit": UNIT,
                       "h2d_bytes_per_step": int(sum(h.numel() * 4 for h in h_in)),
                       "d2h_bytes_per_step": int(J.numel() * 4), "ms_per_step": round(ms_e / e2e_steps, 3),
-                      "overlap": "inputs of step k+1 uploaded on a second stream during step k; J double-buffered "
-                                 "and read back on a third stream"}
-        # the host link alone: the same pinned copies with nothing else running
-        la = torch.cuda.Event(enable_timing=True)
-        lb = torch.cuda.Event(enable_timing=True)
-        la.record(cs)
-        with torch.cuda.stream(cs):
-            for h, t in zip(h_in, sets[0]):
-                t.copy_(h, non_blocking=True)
-        lb.record(cs)
-        torch.cuda.synchronize()
-        res["e2e"]["h2d_alone_gbs"] = round(res["e2e"]["h2d_bytes_per_step"] / (la.elapsed_time(lb) * 1e-3) / 1e9, 1)
+                      "overlap": f"inputs of step k+1 uploaded on {UPLOAD_STREAMS} streams during step k; J "
+                                 "double-buffered and read back on its own stream"}
+
+        # the host link alone: the same pinned copies with nothing else running,
+        # on one stream and on the upload streams
+        def h2d_alone(streams):
+            la = torch.cuda.Event(enable_timing=True)
+            lb = torch.cuda.Event(enable_timing=True)
+            la.record(streams[0])
+            ends = []
+            for u, cs in enumerate(streams):
+                cs.wait_event(la)
+                with torch.cuda.stream(cs):
+                    for f in range(u, len(h_in), len(streams)):
+                        sets[0][f].copy_(h_in[f], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs)
+                ends.append(ev)
+            for ev in ends:
+                streams[0].wait_event(ev)
+            lb.record(streams[0])
+            torch.cuda.synchronize()
+            return round(res["e2e"]["h2d_bytes_per_step"] / (la.elapsed_time(lb) * 1e-3) / 1e9, 1)
+
+        res["e2e"]["h2d_alone_gbs"] = h2d_alone(ups)
+        res["e2e"]["h2d_alone_one_stream_gbs"] = h2d_alone(ups[:1])
         del h_in, h_J, sets, Jb
     del pos, vel, q, kp, payload, out, J, ws_s, ws_d
     torch.cuda.empty_cache()
