@@ -20,14 +20,11 @@
 // Tiled path ("How a tile deposit runs", "Halo sizing", "Correctness is
 // independent of the halo").  The particles are sorted by the tile of their
 // previous position (the page keys on min(i, i_prev) to put the whole halo on
-// the high side; the previous cell is at most one cell above that minimum, so a
-// halo of 2 on both sides holds every stencil of a particle that has not left
-// its tile).  Each CTA owns a fixed-size chunk of the sorted array; for every
-// tile segment inside it, it zeroes a 3 x (T + 4)^3 scratch window in shared
-// memory, adds each particle's edges there with shared-memory reductions when
-// its 3 x 3 x 3 node footprint fits the window, or sends the whole particle to
-// J with global reductions when it does not (the escape valve), and flushes
-// the window once.
+// the high side; here every segment whose cell lies outside the tile goes to J
+// directly, so the key needs no such shift).  A particle whose 3 x 3 x 3 node
+// footprint leaves the window of a 2-cell halo around its tile is counted as an
+// escape, as the page's escape valve defines it.  The kernel itself is
+// described above zigzag_cells_kernel.
 #include "deposit_tiled.cuh"
 
 namespace pcg {
@@ -188,173 +185,360 @@ __global__ void __launch_bounds__(256)
     warp_add_u64(ctr.n_invalid, n_inv);
 }
 
-// General path of one particle in a tile segment: the full split, then its
-// 12 or 24 edges into the scratch window when its 3 x 3 x 3 footprint fits,
-// else into J (the escape valve).  Out of line: it serves the cell-crossing
-// particles, which the hot loop of the tiled kernel only lists.
-template <int TILE, int HALO>
-__device__ __noinline__ void zigzag_general(const Geom g, const ZParticles P, long long p, float inv_dt,
-                                            float *scratch, float *J, int ox, int oy, int oz, unsigned *n_esc) {
-    using C = dep::TileCfg<3, 1, TILE, HALO>;
-    constexpr int TE = C::TE;
-    float x1[3], x2[3], q;
-    load_particle(P, p, x1, x2, q);
-    Zig z;
-    if (!zigzag_split(g, x1, x2, q, inv_dt, z)) return;  // counted by the caller
-    const int lx = dep::local_index<3, TILE, HALO>(z.base[0], ox, g.N[0]);
-    const int ly = dep::local_index<3, TILE, HALO>(z.base[1], oy, g.N[1]);
-    const int lz = dep::local_index<3, TILE, HALO>(z.base[2], oz, g.N[2]);
-    const bool fits = (lx >= -HALO) & (lx + 2 < TILE + HALO) & (ly >= -HALO) & (ly + 2 < TILE + HALO) &
-                      (lz >= -HALO) & (lz + 2 < TILE + HALO);
-    if (!fits) {
-        ++*n_esc;
-        zigzag_global(g, J, z);
-        return;
-    }
-    const int b0 = ((lz + HALO) * TE + (ly + HALO)) * TE + (lx + HALO);
-    if (!PCG_IN(b0, C::CELLS) || !PCG_IN(b0 + (2 * TE + 2) * TE + 2, C::CELLS)) return;
-    float *w0 = scratch + b0;
-    zigzag_edges(z, [&](int c, int dx, int dy, int dz, float v) {
-        red_shared_add_f32(w0 + c * C::CELLS + (dz * TE + dy) * TE + dx, v);
-    });
+// ---------------------------------------------------------------------------
+// Tiled kernel.  A particle's zigzag current is the sum of its segments' (one
+// straight segment when it stays in its cell, the two relay segments when it
+// crosses a face), and a segment with midpoint m (relative to its cell), move D
+// and flux F = q D / dt adds to the c-edges of its cell at cell + a e_u + b e_v
+//   F^c (w_a(m^u) w_b(m^v) + (a == b ? 1 : -1) D^u D^v / 12),
+// which depends on the segment only through four sums per component:
+//   S0 = sum F^c, Su = sum F^c m^u, Sv = sum F^c m^v,
+//   Q = sum F^c (m^u m^v + D^u D^v / 12),
+// giving the edges (a, b) = (0, 0): S0 - Su - Sv + Q, (1, 0): Su - Q,
+// (0, 1): Sv - Q, (1, 1): Q.  So one thread per cell of the 8^3 tile keeps its
+// cell's 12 sums in registers for the whole tile segment, as the CIC kernel
+// does with its corner moments.
+//
+// One persistent CTA of 512 threads per SM walks the chunks b, b + grid, ... of
+// the array sorted by the tile of the previous position, in rounds of 4096
+// particles (8 per thread, float4 loads per field, the next round loaded into
+// registers before this one is accumulated).  A round's segments are placed by
+// rank (a shared u32 counting atomic) into per-cell lists st[pair][rank][cell]
+// that the cell threads read conflict-free.  Particles that stay in one of the
+// tile's cells take the fast path (one segment, a few multiplies); the others
+// (crossing a face, about 11 % at v ~ N(0, 0.05^2); invalid; outside the tile)
+// are queued per warp and taken one per lane after the warp's placements: the
+// full relay split, each segment listed when its cell is one of the tile's, or
+// added to J with global reductions.  At a tile segment's end every cell thread
+// stores its 12 edge values, and one thread per edge adds the <= 4 cells' values
+// that meet there and issues one global reduction.  No shared-memory float
+// atomics: on this GPU they are a serial read-modify-write.
+struct ZzCfg {
+    static constexpr int THREADS = 512;
+    static constexpr int NC = 512;                // cells of an 8^3 tile, one thread each
+    static constexpr int PPT = 8;                 // particles per thread per round
+    static constexpr int R = THREADS * PPT;       // round size
+    static constexpr int CAP = 14;                // listed segments per cell and round
+    static constexpr int QCAP = PPT * 32;         // queued particles per warp and round: room for all
+    static constexpr size_t LIST = (size_t)CAP * NC;
+    static constexpr size_t SMEM = LIST * 3 * 8 + LIST * 4 + (size_t)(THREADS / 32) * QCAP * 4 + (size_t)NC * 4;
+    static_assert(THREADS == NC, "one thread per cell");
+    static_assert((size_t)12 * NC * 4 <= LIST * 3 * 8, "the edge values fit in the list area");
+};
+
+// List a segment of tile-local cell `cell` (midpoint m, move D, q / dt):
+// false when the cell's list is full.
+__device__ __forceinline__ bool zz_list(float2 *st, float *sq, unsigned *cnt, int cell, float mx, float my,
+                                        float mz, float Dx, float Dy, float Dz, float qdt) {
+    using K = ZzCfg;
+    if (!PCG_IN(cell, K::NC)) return false;
+    const unsigned r = atomicAdd(&cnt[cell], 1u);
+    if (r >= (unsigned)K::CAP) return false;
+    float2 *e = st + (size_t)r * K::NC + cell;
+    e[0] = make_float2(mx, my);
+    e[K::LIST] = make_float2(mz, Dx);
+    e[2 * K::LIST] = make_float2(Dy, Dz);
+    sq[(size_t)r * K::NC + cell] = qdt;
+    return true;
 }
 
-// Tiled kernel.  Each round gives every thread one particle.  A particle that
-// stays inside its cell moves along a straight line, so its two zigzag
-// segments add up to the single-segment current: with f1, f2 its offsets in
-// the cell, D = f2 - f1, m = (f1 + f2) / 2 and F = q D / dt, the c-edges at
-// (cell + a e_u + b e_v) get F^c (w_a(m^u) w_b(m^v) + (a == b ? 1 : -1) D^u D^v / 12),
-// 12 shared reductions from a few multiplies.  Particles that cross a cell
-// face (about 11 % at v ~ N(0, 0.05^2)) are only listed, and taken after the
-// loop by the general path in compact warps, so that the loop's warps stay
-// converged and issue 12 reductions per particle instead of 24.
-constexpr int kCrossCap = 2048;
-
-template <int TILE, int HALO>
-__global__ void __launch_bounds__(256, 3)
-    zigzag_tiled_kernel(Geom g, ZParticles P, long long n, float inv_dt, const uint32_t *__restrict__ offs,
-                        const unsigned *__restrict__ chunk_tile, long long chunk, float *__restrict__ J,
-                        Counters ctr) {
-    using C = dep::TileCfg<3, 1, TILE, HALO>;
-    constexpr int TE = C::TE;
-    extern __shared__ __align__(16) float scratch[];  // [3][CELLS]
-    __shared__ unsigned cross[kCrossCap];             // segment-relative indices of crossing particles
-    __shared__ unsigned n_cross;
-
-    const int lane = threadIdx.x & 31;
-    const long long c0 = (long long)blockIdx.x * chunk;
-    const long long c1 = min(n, c0 + chunk);
-    unsigned n_esc = 0, n_inv = 0;
-    unsigned t = chunk_tile[blockIdx.x];
-    if (t > g.n_tiles) t = g.n_tiles;
-    for (;; ++t) {
-        long long s = (long long)offs[t];
-        if (s < c0) s = c0;
-        if (s >= c1) break;
-        long long e = (t < g.n_tiles) ? (long long)offs[t + 1] : c1;
-        if (e > c1) e = c1;
-        if (t == g.n_tiles) {
-            // tail pass: slots after the last tile go straight to J
-            for (long long p = s + threadIdx.x; p < e; p += 256) {
-                float x1[3], x2[3], q;
-                load_particle(P, p, x1, x2, q);
-                Zig z;
-                if (!zigzag_split(g, x1, x2, q, inv_dt, z)) {
-                    ++n_inv;
-                    continue;
-                }
-                zigzag_global(g, J, z);
+// The 12 edges of one segment of global cell (cx, cy, cz) (each in [-1, N]) into
+// J with global reductions (periodic wrap).
+__device__ __forceinline__ void zz_segment_global(const Geom &g, float *__restrict__ J, int cx, int cy, int cz,
+                                                  const float (&m)[3], const float (&D)[3], float qdt) {
+    const int cell[3] = {cx, cy, cz};
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const int u = (c + 1) % 3, v = (c + 2) % 3;
+        const float F = qdt * D[c];
+        const float Su = F * m[u], Sv = F * m[v];
+        const float Q = F * (m[u] * m[v] + D[u] * D[v] * (1.f / 12.f));
+        const float val[2][2] = {{F - Su - Sv + Q, Su - Q}, {Sv - Q, Q}};  // [b][a]
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int a = 0; a < 2; ++a) {
+                int nd[3] = {cell[0], cell[1], cell[2]};
+                nd[u] += a;
+                nd[v] += b;
+                const int gx = wrap_once(nd[0], g.N[0]), gy = wrap_once(nd[1], g.N[1]),
+                          gz = wrap_once(nd[2], g.N[2]);
+                const long long node = ((long long)gz * g.N[1] + gy) * g.N[0] + gx;
+                if (PCG_IN(node, g.ncells)) red_add_f32(J + c * g.ncells + node, val[b][a]);
             }
-            break;
+    }
+}
+
+// The general path of a queued particle of the tile at (ox, oy, oz): the full
+// relay split; each segment listed when its cell is one of the tile's (list
+// not full), else added to J.  Returns 1 invalid (skipped), 2 escaped (its
+// 3 x 3 x 3 node footprint leaves the window [-HALO, 8 + HALO) of the tile, the
+// escape valve's definition), 0 otherwise.
+template <int HALO>
+__device__ __forceinline__ int zz_slow(const Geom &g, float *J, float2 *st, float *sq, unsigned *cnt, int ox,
+                                       int oy, int oz, const float (&x1)[3], const float (&x2)[3], float q,
+                                       float inv_dt) {
+    Zig z;
+    if (!zigzag_split(g, x1, x2, q, inv_dt, z)) return 1;
+    const int lx = dep::local_index<3, 8, HALO>(z.base[0], ox, g.N[0]);
+    const int ly = dep::local_index<3, 8, HALO>(z.base[1], oy, g.N[1]);
+    const int lz = dep::local_index<3, 8, HALO>(z.base[2], oz, g.N[2]);
+    const bool fits = (lx >= -HALO) & (lx + 2 < 8 + HALO) & (ly >= -HALO) & (ly + 2 < 8 + HALO) &
+                      (lz >= -HALO) & (lz + 2 < 8 + HALO);
+    const float qdt = q * inv_dt;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const int cx = z.base[0] + z.cell[s][0], cy = z.base[1] + z.cell[s][1], cz = z.base[2] + z.cell[s][2];
+        const unsigned dx = (unsigned)(cx - ox), dy = (unsigned)(cy - oy), dz = (unsigned)(cz - oz);
+        if ((dx < 8u) & (dy < 8u) & (dz < 8u) &&
+            zz_list(st, sq, cnt, ((int)dz * 8 + (int)dy) * 8 + (int)dx, z.W[s][0], z.W[s][1], z.W[s][2],
+                    z.D[s][0], z.D[s][1], z.D[s][2], qdt))
+            continue;
+        const float m[3] = {z.W[s][0], z.W[s][1], z.W[s][2]};
+        const float D[3] = {z.D[s][0], z.D[s][1], z.D[s][2]};
+        zz_segment_global(g, J, cx, cy, cz, m, D, qdt);
+    }
+    return fits ? 0 : 2;
+}
+
+template <int HALO>
+__global__ void __launch_bounds__(512, 1)
+    zigzag_cells_kernel(Geom g, ZParticles P, long long n, float inv_dt, const uint32_t *__restrict__ offs,
+                        const unsigned *__restrict__ chunk_tile, long long chunk, long long nchunks,
+                        float *__restrict__ J, Counters ctr, bool vec) {
+    using K = ZzCfg;
+    constexpr int NC = K::NC, CAP = K::CAP, QCAP = K::QCAP;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    float2 *st = reinterpret_cast<float2 *>(dsm);                                 // [3][CAP][NC]
+    float *sq = reinterpret_cast<float *>(st + 3 * K::LIST);                      // [CAP][NC]: q / dt
+    int *qbuf = reinterpret_cast<int *>(sq + K::LIST);                            // [warps][QCAP]
+    unsigned *cnt = reinterpret_cast<unsigned *>(qbuf + (K::THREADS / 32) * QCAP);  // [NC]
+
+    const int tid = threadIdx.x, lane = tid & 31;
+    int *wq = qbuf + (tid >> 5) * QCAP;
+    unsigned n_esc = 0, n_inv = 0;
+    cnt[tid] = 0;
+    float acc[3][4];  // per component: S0, Su, Sv, Q
+#pragma unroll
+    for (int c = 0; c < 3; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+
+    // the particles of one round, this thread's 8 slots
+    float A[3][8], B[3][8], Q[8];  // previous position, position, charge
+    auto load_round = [&](const dep::RoundPos &r) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long b = r.rb + h * (K::R / 2) + 4 * tid;
+            if (vec && b + 3 < n) {
+#pragma unroll
+                for (int mu = 0; mu < 3; ++mu) {
+                    const float4 a = *reinterpret_cast<const float4 *>(P.x1[mu] + b);
+                    const float4 c = *reinterpret_cast<const float4 *>(P.x2[mu] + b);
+                    A[mu][4 * h] = a.x; A[mu][4 * h + 1] = a.y; A[mu][4 * h + 2] = a.z; A[mu][4 * h + 3] = a.w;
+                    B[mu][4 * h] = c.x; B[mu][4 * h + 1] = c.y; B[mu][4 * h + 2] = c.z; B[mu][4 * h + 3] = c.w;
+                }
+                const float4 q = *reinterpret_cast<const float4 *>(P.q + b);
+                Q[4 * h] = q.x; Q[4 * h + 1] = q.y; Q[4 * h + 2] = q.z; Q[4 * h + 3] = q.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const long long p = (b + j < n) ? b + j : 0;
+#pragma unroll
+                    for (int mu = 0; mu < 3; ++mu) {
+                        A[mu][4 * h + j] = P.x1[mu][p];
+                        B[mu][4 * h + j] = P.x2[mu][p];
+                    }
+                    Q[4 * h + j] = P.q[p];
+                }
+            }
         }
-        if (e <= s) continue;  // empty tile
-        const int tx = (int)(t % (unsigned)g.nt[0]);
-        const int ty = (int)((t / (unsigned)g.nt[0]) % (unsigned)g.nt[1]);
-        const int tz = (int)(t / ((unsigned)g.nt[0] * (unsigned)g.nt[1]));
-        const int ox = tx * TILE, oy = ty * TILE, oz = tz * TILE;
+    };
+    // slots after the last tile: the flat path, straight to J
+    auto tail = [&](const dep::RoundPos &r) {
+        for (long long p = r.lo + tid; p < r.hi; p += K::THREADS) {
+            float x1[3], x2[3], q;
+            load_particle(P, p, x1, x2, q);
+            Zig z;
+            if (!zigzag_split(g, x1, x2, q, inv_dt, z)) {
+                ++n_inv;
+                continue;
+            }
+            zigzag_global(g, J, z);
+        }
+    };
 
-        for (int i = threadIdx.x; i < C::FLOATS; i += 256) scratch[i] = 0.f;
-        if (threadIdx.x == 0) n_cross = 0;
-        __syncthreads();
-
-        for (long long r = s; r < e; r += 256) {
-            const long long p = r + threadIdx.x;
-            const bool live = p < e;
-            float x1[3], x2[3], q = 0.f;
-            if (live) load_particle(P, p, x1, x2, q);
-            bool ok = live, same = true;
+    dep::RoundPos cur;
+    dep::seek(g, offs, chunk_tile, n, chunk, nchunks, blockIdx.x, 0xffffffffu, cur);
+    while (cur.t == g.n_tiles) {  // a chunk that holds only invalid-tail particles
+        tail(cur);
+        dep::seek(g, offs, chunk_tile, n, chunk, nchunks, cur.c + gridDim.x, 0xffffffffu, cur);
+    }
+    if (cur.t > g.n_tiles) {
+        warp_add_u64(ctr.n_invalid, n_inv);
+        return;
+    }
+    load_round(cur);
+    __syncthreads();  // counters zeroed
+    auto slow_count = [&](int rc) {
+        n_inv += rc == 1;
+        n_esc += rc == 2;
+    };
+    const unsigned lanes_below = (1u << lane) - 1u;
+    while (true) {
+        const int tx = (int)(cur.t % (unsigned)g.nt[0]);
+        const int ty = (int)((cur.t / (unsigned)g.nt[0]) % (unsigned)g.nt[1]);
+        const int tz = (int)(cur.t / ((unsigned)g.nt[0] * (unsigned)g.nt[1]));
+        const int ox = tx * 8, oy = ty * 8, oz = tz * 8;
+        // ---- place the round held in registers: one straight segment for a
+        // particle that stays in one of the tile's cells ----
+        int qn = 0;  // particles this warp has queued this round (warp-uniform)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const long long p = cur.rb + (j >> 2) * (K::R / 2) + 4 * tid + (j & 3);
+            const bool live = p >= cur.lo && p < cur.hi;
+            bool fast = live;
             int ic[3];
             float f1[3], f2[3];
 #pragma unroll
             for (int mu = 0; mu < 3; ++mu) {
-                const float a1 = live ? x1[mu] : 0.f, a2 = live ? x2[mu] : 0.f;
-                ok &= (a1 >= 0.f) & (a1 < g.Nf[mu]) & (a2 >= 0.f) & (a2 < g.Nf[mu]);
+                const float a1 = A[mu][j], a2 = B[mu][j];
+                // both positions in [0, N) (a NaN fails) and in the same cell
+                fast &= (a1 >= 0.f) & (a1 < g.Nf[mu]) & (a2 >= 0.f) & (a2 < g.Nf[mu]);
                 const int i1 = (int)a1, i2 = (int)a2;
-                int di = i2 - i1;
-                if (2 * di > g.N[mu]) di -= g.N[mu];
-                if (2 * di < -g.N[mu]) di += g.N[mu];
-                ok &= (di >= -1) & (di <= 1);
-                same &= di == 0;
+                fast &= i1 == i2;
                 ic[mu] = i1;
                 f1[mu] = a1 - (float)i1;
                 f2[mu] = a2 - (float)i2;
             }
-            n_inv += live & !ok;
-            const bool crossing = ok & !same;
-            const unsigned m = __ballot_sync(0xffffffffu, crossing);
-            if (m != 0u) {
-                unsigned base = 0;
-                if (lane == 0) base = atomicAdd(&n_cross, (unsigned)__popc(m));
-                base = __shfl_sync(0xffffffffu, base, 0);
-                if (crossing) {
-                    const unsigned slot = base + __popc(m & ((1u << lane) - 1u));
-                    if (slot < kCrossCap) cross[slot] = (unsigned)(p - s);
-                    else zigzag_general<TILE, HALO>(g, P, p, inv_dt, scratch, J, ox, oy, oz, &n_esc);
-                }
+            const unsigned dx = (unsigned)(ic[0] - ox), dy = (unsigned)(ic[1] - oy), dz = (unsigned)(ic[2] - oz);
+            fast &= (dx < 8u) & (dy < 8u) & (dz < 8u);
+            bool slow = live;
+            if (fast) {
+                const float qdt = Q[j] * inv_dt;
+                slow = !zz_list(st, sq, cnt, ((int)dz * 8 + (int)dy) * 8 + (int)dx, 0.5f * (f1[0] + f2[0]),
+                                0.5f * (f1[1] + f2[1]), 0.5f * (f1[2] + f2[2]), f2[0] - f1[0], f2[1] - f1[1],
+                                f2[2] - f1[2], qdt);
             }
-            if (!(ok & same)) continue;
-            const int lx = dep::local_index<2, TILE, HALO>(ic[0], ox, g.N[0]);
-            const int ly = dep::local_index<2, TILE, HALO>(ic[1], oy, g.N[1]);
-            const int lz = dep::local_index<2, TILE, HALO>(ic[2], oz, g.N[2]);
-            const bool fits = (lx >= -HALO) & (lx + 1 < TILE + HALO) & (ly >= -HALO) & (ly + 1 < TILE + HALO) &
-                              (lz >= -HALO) & (lz + 1 < TILE + HALO);
-            if (!fits) {
-                zigzag_general<TILE, HALO>(g, P, p, inv_dt, scratch, J, ox, oy, oz, &n_esc);
-                continue;
+            const unsigned m = __ballot_sync(0xffffffffu, slow);
+            if (m) {  // warp-uniform
+                const int at = qn + __popc(m & lanes_below);
+                if (slow && PCG_IN(at, QCAP)) wq[at] = (int)(p - cur.rb);
+                qn += __popc(m);
             }
-            float D[3], mid[3], F[3];
-#pragma unroll
-            for (int mu = 0; mu < 3; ++mu) {
-                D[mu] = f2[mu] - f1[mu];
-                mid[mu] = 0.5f * (f1[mu] + f2[mu]);
-                F[mu] = q * D[mu] * inv_dt;
+        }
+        // the warp's queue, one particle per lane: re-read from memory (it was
+        // loaded one round ago and sits in L2), then the general path
+        __syncwarp();
+        for (int e = lane; e < qn; e += 32) {
+            const long long pp = cur.rb + wq[e];
+            if (!PCG_IN(pp, n)) continue;
+            float x1[3], x2[3], q;
+            load_particle(P, pp, x1, x2, q);
+            slow_count(zz_slow<HALO>(g, J, st, sq, cnt, ox, oy, oz, x1, x2, q, inv_dt));
+        }
+        __syncwarp();
+        // ---- the next round: position, and its particles into registers ----
+        dep::RoundPos nxt = cur;
+        nxt.rb = cur.rb + K::R;
+        if (nxt.rb >= cur.hi) dep::seek(g, offs, chunk_tile, n, chunk, nchunks, cur.c, cur.t + 1, nxt);
+        const bool tile_ends = nxt.t != cur.t || nxt.c != cur.c;
+        const bool more = nxt.t < g.n_tiles;
+        // issued before the barrier, so that the warps issue them as they finish placing
+        if (more) load_round(nxt);
+        __syncthreads();  // the round is listed
+
+        // ---- every cell's thread adds its listed segments' sums ----
+        {
+            const unsigned m0 = cnt[tid];
+            const unsigned m = m0 < (unsigned)CAP ? m0 : (unsigned)CAP;
+            cnt[tid] = 0;
+#pragma unroll 2
+            for (unsigned r = 0; r < m; ++r) {
+                const float2 a = st[(size_t)r * NC + tid];
+                const float2 b = st[K::LIST + (size_t)r * NC + tid];
+                const float2 c = st[2 * K::LIST + (size_t)r * NC + tid];
+                const float qdt = sq[(size_t)r * NC + tid];
+                const float mx = a.x, my = a.y, mz = b.x, Dx = b.y, Dy = c.x, Dz = c.y;
+                const float Fx = qdt * Dx, Fy = qdt * Dy, Fz = qdt * Dz;
+                // per component c (u, v the next two axes): m^u m^v + D^u D^v / 12
+                const float pyz = fmaf(Dy * Dz, 1.f / 12.f, my * mz);
+                const float pzx = fmaf(Dz * Dx, 1.f / 12.f, mz * mx);
+                const float pxy = fmaf(Dx * Dy, 1.f / 12.f, mx * my);
+                acc[0][0] += Fx;
+                acc[0][1] = fmaf(Fx, my, acc[0][1]);
+                acc[0][2] = fmaf(Fx, mz, acc[0][2]);
+                acc[0][3] = fmaf(Fx, pyz, acc[0][3]);
+                acc[1][0] += Fy;
+                acc[1][1] = fmaf(Fy, mz, acc[1][1]);
+                acc[1][2] = fmaf(Fy, mx, acc[1][2]);
+                acc[1][3] = fmaf(Fy, pzx, acc[1][3]);
+                acc[2][0] += Fz;
+                acc[2][1] = fmaf(Fz, mx, acc[2][1]);
+                acc[2][2] = fmaf(Fz, my, acc[2][2]);
+                acc[2][3] = fmaf(Fz, pxy, acc[2][3]);
             }
-            const int b0 = ((lz + HALO) * TE + (ly + HALO)) * TE + (lx + HALO);
-            if (!PCG_IN(b0, C::CELLS) || !PCG_IN(b0 + (TE + 1) * TE + 1, C::CELLS)) continue;
-            float *w0 = scratch + b0;
+        }
+        if (tile_ends) {
+            // every cell's 12 edge values to the free list area with plain stores;
+            // after a barrier one thread per edge adds the <= 4 cells' values that
+            // meet there and reduces the total into J once
+            float *edge = reinterpret_cast<float *>(st);  // [3][4][NC]: (c, b * 2 + a)
+            __syncthreads();  // every list has been read
 #pragma unroll
             for (int c = 0; c < 3; ++c) {
-                const int u = (c + 1) % 3, v = (c + 2) % 3;
-                const float wu = mid[u], wv = mid[v];
-                const float avg = D[u] * D[v] * (1.f / 12.f);
-                const float val[2][2] = {{F[c] * ((1.f - wu) * (1.f - wv) + avg), F[c] * (wu * (1.f - wv) - avg)},
-                                         {F[c] * ((1.f - wu) * wv - avg), F[c] * (wu * wv + avg)}};
-                // the edge at cell + a e_u + b e_v
-                constexpr int stride[3] = {1, TE, TE * TE};
+                const float S0 = acc[c][0], Su = acc[c][1], Sv = acc[c][2], Qc = acc[c][3];
+                edge[(c * 4 + 0) * NC + tid] = S0 - Su - Sv + Qc;
+                edge[(c * 4 + 1) * NC + tid] = Su - Qc;
+                edge[(c * 4 + 2) * NC + tid] = Sv - Qc;
+                edge[(c * 4 + 3) * NC + tid] = Qc;
+                acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+            }
+            __syncthreads();
+            // component c's edges start at the nodes [0, 8) along c and [0, 9)
+            // along u and v (the edge at node n belongs to cells n - a e_u - b e_v)
+            constexpr int NE = 8 * 9 * 9;
+            for (int idx = tid; idx < 3 * NE; idx += K::THREADS) {
+                const int c = idx / NE, r = idx - c * NE;
+                const int u = c == 2 ? 0 : c + 1, v = c == 0 ? 2 : (c == 1 ? 0 : 1);
+                const int nc = r % 8, nu = (r / 8) % 9, nv = r / 72;
+                float sum = 0.f;
 #pragma unroll
                 for (int b = 0; b < 2; ++b)
 #pragma unroll
-                    for (int a = 0; a < 2; ++a)
-                        red_shared_add_f32(w0 + c * C::CELLS + a * stride[u] + b * stride[v], val[b][a]);
+                    for (int a = 0; a < 2; ++a) {
+                        const int cu = nu - a, cv = nv - b;
+                        if (cu < 0 || cu >= 8 || cv < 0 || cv >= 8) continue;
+                        int cell3[3];
+                        cell3[c] = nc;
+                        cell3[u] = cu;
+                        cell3[v] = cv;
+                        const int cell = (cell3[2] * 8 + cell3[1]) * 8 + cell3[0];
+                        sum += edge[(c * 4 + b * 2 + a) * NC + cell];
+                    }
+                if (sum == 0.f) continue;
+                int nd[3];
+                nd[c] = nc;
+                nd[u] = nu;
+                nd[v] = nv;
+                int gx = ox + nd[0], gy = oy + nd[1], gz = oz + nd[2];
+                while (gx >= g.N[0]) gx -= g.N[0];
+                while (gy >= g.N[1]) gy -= g.N[1];
+                while (gz >= g.N[2]) gz -= g.N[2];
+                const long long node = ((long long)gz * g.N[1] + gy) * g.N[0] + gx;
+                if (PCG_IN(node, g.ncells)) red_add_f32(J + c * g.ncells + node, sum);
             }
         }
-        __syncthreads();
-        const unsigned nc = min(n_cross, (unsigned)kCrossCap);
-        for (unsigned i = threadIdx.x; i < nc; i += 256)
-            zigzag_general<TILE, HALO>(g, P, s + cross[i], inv_dt, scratch, J, ox, oy, oz, &n_esc);
-        __syncthreads();
-        dep::flush_scratch<3, TILE, HALO, 256>(g, scratch, J, ox, oy, oz);
-        __syncthreads();
+        if (!more) {
+            // the invalid tail sits at the end of the array: after it come only
+            // chunks that are all tail or past the end
+            dep::RoundPos rr = nxt;
+            while (rr.t == g.n_tiles) {
+                tail(rr);
+                dep::seek(g, offs, chunk_tile, n, chunk, nchunks, rr.c + gridDim.x, 0xffffffffu, rr);
+            }
+            break;
+        }
+        cur = nxt;
+        __syncthreads();  // lists, counters and edge values read
     }
     warp_add_u64(ctr.n_escaped, n_esc);
     warp_add_u64(ctr.n_invalid, n_inv);
@@ -406,10 +590,15 @@ extern "C" pcg_status pcg_deposit_zigzag(const int32_t *grid, int32_t tile, int6
         zigzag_flat_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, s>>>(g, P, n, inv_dt, J, ctr);
         return launch_status();
     }
-    using C = dep::TileCfg<3, 1, 8, 2>;
-    const size_t smem = C::FLOATS * sizeof(float);
+    bool vec = true;
+    for (int mu = 0; mu < 3; ++mu) vec = vec && aligned16(P.x1[mu]) && aligned16(P.x2[mu]);
+    vec = vec && aligned16(P.q);
+    const long long sms = num_sms();
+    const unsigned grid_ = (unsigned)(nchunks < sms ? nchunks : sms);
+    PCG_CHECK_CUDA(cudaFuncSetAttribute(zigzag_cells_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)ZzCfg::SMEM));
     prof::Mark mk("deposit_zigzag", s);
-    zigzag_tiled_kernel<8, 2><<<(unsigned)nchunks, 256, smem, s>>>(g, P, n, inv_dt, tile_offsets, chunk_tile, chunk,
-                                                                    J, ctr);
+    zigzag_cells_kernel<2><<<grid_, ZzCfg::THREADS, ZzCfg::SMEM, s>>>(g, P, n, inv_dt, tile_offsets, chunk_tile,
+                                                                       chunk, nchunks, J, ctr, vec);
     return launch_status();
 }
