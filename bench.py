@@ -548,7 +548,7 @@ def cpu_threads_for(d):
     return min(cpu["usable"], fit), cpu
 
 
-def cpu_baseline_current(d, budget_s=8.0):
+def cpu_baseline_current(d, target_s=8.0):
     """The fp64 oracle as it stands on bounded samples of the same workload:
     one thread, then the same calls spread over the host's cores."""
     import oracle
@@ -558,7 +558,7 @@ def cpu_baseline_current(d, budget_s=8.0):
     oracle.deposit_current(d["grid"], d["order"], [p[:s0] for p in d["pos"]], [v[:s0] for v in d["vel"]],
                            d["q"][:s0])
     t0 = time.perf_counter() - t
-    s = int(min(n, max(s0, s0 * budget_s / max(t0, 1e-3))))
+    s = int(min(n, max(s0, s0 * target_s / max(t0, 1e-3))))
     t = time.perf_counter()
     oracle.deposit_current(d["grid"], d["order"], [p[:s] for p in d["pos"]], [v[:s] for v in d["vel"]],
                            d["q"][:s])
@@ -830,8 +830,8 @@ def run_reference(args):
     t = time.perf_counter()
     oracle.deposit_current(d["grid"], 1, [p[:s0] for p in d["pos"]], [v[:s0] for v in d["vel"]], d["q"][:s0])
     rate = s0 / (time.perf_counter() - t)
-    budget = 90.0  # seconds for the whole --steps/--warmup run
-    s = int(max(20_000 * threads, min(n, rate * threads * budget / total)))
+    target_s = 90.0  # seconds for the whole --steps/--warmup run
+    s = int(max(20_000 * threads, min(n, rate * threads * target_s / total)))
 
     def step(k):
         a0 = (k * s) % n

@@ -193,7 +193,7 @@ PCG_API pcg_status pcg_tile_sort(int32_t dim, const int32_t *grid, int32_t tile,
  * {j, j+1, j+2}), deposited as in "Tiled current deposit" (Entity wiki),
  * sections "How a tile deposit runs" (one team per tile, a haloed
  * (T + 2*HALO)^D x 3 scratch tile, the fit test, a single flush per scratch
- * cell), "Halo sizing" (HALO = stencil reach + drift budget) and "Correctness
+ * cell), "Halo sizing" (HALO = stencil reach + drift allowance) and "Correctness
  * is independent of the halo" (a particle whose stencil leaves the scratch
  * window is deposited whole into J through global atomics).
  *
